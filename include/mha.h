@@ -1,0 +1,187 @@
+/*
+ * mha.h -- C ABI of the GB300 (sm_103a) multi-head attention forward library.
+ *
+ * The operation is the forward pass of the Transformer's multi-head attention
+ * sublayer, as the pages define it:
+ *
+ *   "003-Transformer" tutorial, section "Multi-head attention",
+ *   MultiHeadedAttention.forward(query, key, value, mask):
+ *     Q = query W_q^T + b_q, K = key W_k^T + b_k, V = value W_v^T + b_v
+ *         (nn.Linear(d_model, d_model), weights stored [out, in]);
+ *     each viewed as (B, L, h, d_k) and transposed to (B, h, L, d_k), so head i
+ *         owns features [i*d_k, (i+1)*d_k), with d_k = d_model / h;
+ *     per head: "The Annotated Transformer", section "Attention", attention():
+ *         scores = Q K^T / sqrt(d_k); scores.masked_fill(mask == 0, -1e9);
+ *         p_attn = softmax(scores, dim=-1); head = p_attn V;
+ *     heads transposed back and concatenated to (B, L_q, h*d_k);
+ *     out = concat W_o^T + b_o.
+ *
+ * Mask (1 = may attend): the AND of up to three parts, broadcast over heads
+ * (mask.unsqueeze(1) in MultiHeadedAttention.forward):
+ *   causal          key j allowed for query i iff j <= i ("The Annotated
+ *                   Transformer", subsequent_mask(); diagonal allowed).
+ *   key_valid_lens  key j allowed iff j < key_valid_lens[b] (d2l
+ *                   MultiHeadAttention valid_lens, d2l Transformer chapter).
+ *   dense           byte mask [B, dense_mq, L_k], dense_mq in {1, L_q};
+ *                   0 = masked; dense_mq == 1 broadcasts over queries.
+ * A masked score is REPLACED by -1e9 after the 1/sqrt(d_k) scaling, so a
+ * query row whose keys are all masked gets uniform weights 1/L_k over all L_k
+ * keys. Dropout is the identity (forward / evaluation).
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers into buffers the caller owns,
+ *     row-major and contiguous, unless an entry point says otherwise. The
+ *     library never allocates or frees device memory and never synchronises
+ *     the stream (except mha_check_device_status, which says so).
+ *   - dt selects the storage type of query/key/value/weights/biases/out and of
+ *     the workspace tensors: MHA_F32 (fp32 everywhere, fp32 SIMT arithmetic,
+ *     any d_k <= 256) or MHA_BF16 (bf16 storage, fp32 accumulation on the
+ *     tensor cores, d_k == 64 only). p_attn is always fp32.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and the call returns without waiting for it.
+ *   - Arguments are validated on the host before anything is enqueued. On a
+ *     non-OK status returned by validation, no output buffer is touched.
+ *     mha_last_error() then gives a message (thread-local).
+ *   - B, L_q, L_k, d_model, h >= 1; d_model % h == 0 (the pages assert
+ *     embedding_dim % head == 0). causal requires L_q == L_k (the subsequent
+ *     mask is square).
+ *   - MHA_BF16 also requires every tensor pointer to be 16-byte aligned.
+ */
+#ifndef GB300_MHA_H
+#define GB300_MHA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MHA_OK = 0,
+    MHA_ERR_INVALID_ARG = 1,   /* bad size, null required pointer, small workspace */
+    MHA_ERR_UNSUPPORTED = 2,   /* valid per the pages but not implemented (e.g. bf16 with d_k != 64) */
+    MHA_ERR_CUDA = 3           /* a CUDA call failed; see mha_last_error() */
+} mha_status_t;
+
+typedef enum { MHA_F32 = 0, MHA_BF16 = 1 } mha_dtype_t;
+
+typedef struct {
+    int causal;                     /* nonzero: subsequent mask, key j <= query i */
+    const int32_t* key_valid_lens;  /* device [B] or NULL: key j allowed iff j < len[b]; len < 0 reads as 0 */
+    const uint8_t* dense;           /* device [B, dense_mq, L_k] or NULL: 0 = masked */
+    int dense_mq;                   /* 1 (broadcast over queries) or L_q; ignored if dense is NULL */
+} mha_mask_t;
+
+/*
+ * Workspace the forward pass needs, in bytes (a multiple of 256).
+ * Layout (each part starts on a 256-byte boundary, element type = dt):
+ *   Qh   [B, h, L_q, d_k]      head-split projected queries
+ *   KVh  [B, 2, h, L_k, d_k]   head-split projected keys (slot 0) and values (slot 1)
+ *   ctx  [B, L_q, d_model]     concatenated head outputs (input of W_o)
+ *   stat [B, h, L_q, 2] fp32   per-row softmax statistics (max, sum) used for p_attn
+ * Returns 0 for invalid sizes.
+ */
+size_t mha_workspace_size(mha_dtype_t dt, int B, int L_q, int L_k, int d_model, int h);
+
+/*
+ * mha_forward -- the whole sublayer: out = MultiHeadedAttention(query, key, value, mask).
+ *   query [B, L_q, d_model]; key, value [B, L_k, d_model]   (may alias each other)
+ *   w_q, w_k, w_v, w_o [d_model, d_model] stored (out, in); b_* [d_model] or NULL (= zero bias)
+ *   mask   NULL = no mask
+ *   out    [B, L_q, d_model], type dt; must not alias any input or the workspace
+ *   p_attn NULL, or fp32 [B, h, L_q, L_k]: the attention weights of every head
+ *          (the pages keep them as self.attn for visualisation)
+ *   workspace >= mha_workspace_size(...) bytes of device memory, 256-byte aligned
+ * Three stages run in order on `stream`: mha_qkv_projection, mha_attention_core,
+ * mha_output_projection.
+ */
+mha_status_t mha_forward(mha_dtype_t dt,
+                         const void* query, const void* key, const void* value,
+                         const void* w_q, const void* b_q,
+                         const void* w_k, const void* b_k,
+                         const void* w_v, const void* b_v,
+                         const void* w_o, const void* b_o,
+                         int B, int L_q, int L_k, int d_model, int h,
+                         const mha_mask_t* mask,
+                         void* out, float* p_attn,
+                         void* workspace, size_t workspace_bytes,
+                         void* stream);
+
+/*
+ * Stage 1 -- the three input projections of MultiHeadedAttention.forward, written
+ * head-split into the workspace (Qh and KVh above). One launch covers all three.
+ */
+mha_status_t mha_qkv_projection(mha_dtype_t dt,
+                                const void* query, const void* key, const void* value,
+                                const void* w_q, const void* b_q,
+                                const void* w_k, const void* b_k,
+                                const void* w_v, const void* b_v,
+                                int B, int L_q, int L_k, int d_model, int h,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Stage 2 -- attention() for every (batch, head): scores, scale, -1e9 fill,
+ * softmax, P.V, written concatenated into ctx of the workspace; and, if p_attn
+ * is not NULL, the normalised weights fp32 [B, h, L_q, L_k]. Reads Qh and KVh.
+ */
+mha_status_t mha_attention_core(mha_dtype_t dt, int B, int L_q, int L_k, int d_model, int h,
+                                const mha_mask_t* mask, float* p_attn,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Stage 3 -- the fourth Linear of MultiHeadedAttention: out = ctx W_o^T + b_o,
+ * reading ctx from the workspace. out [B, L_q, d_model], type dt.
+ */
+mha_status_t mha_output_projection(mha_dtype_t dt, const void* w_o, const void* b_o,
+                                   int B, int L_q, int L_k, int d_model, int h,
+                                   void* out, void* workspace, size_t workspace_bytes,
+                                   void* stream);
+
+/*
+ * mha_forward_host -- the same sublayer with the activations in HOST memory:
+ * query/key/value are read from host buffers and out is written to a host
+ * buffer; weights, biases, mask parts and the workspace are device pointers as
+ * above. The host buffers should be page-locked for the copies to be
+ * asynchronous. `staging` is device memory of at least
+ * mha_host_staging_size(...) bytes that receives the activations. Enqueues:
+ * host->device copies of query (and key, value unless they alias query / each
+ * other), the three stages, and the device->host copy of out; then returns
+ * (the caller synchronises the stream before reading out).
+ */
+size_t mha_host_staging_size(mha_dtype_t dt, int B, int L_q, int L_k, int d_model,
+                             int kv_distinct, int q_distinct);
+mha_status_t mha_forward_host(mha_dtype_t dt,
+                              const void* h_query, const void* h_key, const void* h_value,
+                              const void* w_q, const void* b_q,
+                              const void* w_k, const void* b_k,
+                              const void* w_v, const void* b_v,
+                              const void* w_o, const void* b_o,
+                              int B, int L_q, int L_k, int d_model, int h,
+                              const mha_mask_t* mask,
+                              void* h_out,
+                              void* staging, size_t staging_bytes,
+                              void* workspace, size_t workspace_bytes,
+                              void* stream);
+
+/* Message for the last non-OK status returned on this thread ("" if none). */
+const char* mha_last_error(void);
+
+/*
+ * Device-side status of the bounded waits inside the tensor-core kernels.
+ * Every pipeline wait gives up after a fixed iteration budget instead of
+ * spinning forever; when one gives up, the kernel records a code here and runs
+ * to completion (its outputs are then not valid). This call SYNCHRONISES the
+ * device, copies the word to *status (0 = no wait gave up), and, if reset is
+ * nonzero, clears it.
+ */
+mha_status_t mha_check_device_status(int* status, int reset);
+
+/* Library version string. */
+const char* mha_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300_MHA_H */

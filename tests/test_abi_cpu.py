@@ -1,0 +1,87 @@
+"""The C-ABI library builds, loads and exports every symbol include/mha.h declares;
+host-side validation rejects bad arguments before anything touches a GPU.
+No compute call is made here (no GPU in this test)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from transformer_head_scaled_fwd_gb300 import binding
+from transformer_head_scaled_fwd_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return binding.load()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "mha.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mha_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert set(names) == set(binding.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_version(lib):
+    assert "sm_103a" in binding.version()
+
+
+def test_workspace_size_layout(lib):
+    # bf16: Qh + KVh + ctx + stats, each 256-aligned
+    B_, Lq, Lk, d, h = 2, 10, 7, 512, 8
+    es = 2
+    a = lambda x: (x + 255) // 256 * 256
+    q = a(es * B_ * Lq * d)
+    kv = a(es * B_ * 2 * Lk * d)
+    ctx = a(es * B_ * Lq * d)
+    st = a(4 * 2 * B_ * h * Lq)
+    assert binding.workspace_size(binding.MHA_BF16, B_, Lq, Lk, d, h) == q + kv + ctx + st
+    assert binding.workspace_size(binding.MHA_BF16, B_, Lq, Lk, 510, 8) == 0
+    assert binding.workspace_size(binding.MHA_F32, 0, Lq, Lk, d, h) == 0
+
+
+def _call_forward(lib, dt=binding.MHA_BF16, B_=1, Lq=4, Lk=4, d=128, h=2, mask=None, ws=1 << 30,
+                  ws_ptr=256, ptr=4096):
+    P = ctypes.c_void_p(ptr)
+    return lib.mha_forward(dt, P, P, P, P, None, P, None, P, None, P, None, B_, Lq, Lk, d, h,
+                           ctypes.byref(mask) if mask is not None else None, P, None,
+                           ctypes.c_void_p(ws_ptr), ws, None)
+
+
+def test_validation_without_gpu(lib):
+    assert _call_forward(lib, d=130, h=4) == binding.MHA_ERR_INVALID_ARG          # d % h != 0
+    assert b"d_model % h" in lib.mha_last_error()
+    assert _call_forward(lib, B_=0) == binding.MHA_ERR_INVALID_ARG
+    assert _call_forward(lib, d=256, h=2) == binding.MHA_ERR_UNSUPPORTED          # bf16 d_k = 128
+    assert _call_forward(lib, dt=binding.MHA_F32, d=1024, h=2) == binding.MHA_ERR_UNSUPPORTED
+    assert _call_forward(lib, dt=7) == binding.MHA_ERR_INVALID_ARG
+    m = binding.MaskT(); m.causal = 1
+    assert _call_forward(lib, Lq=4, Lk=5, mask=m) == binding.MHA_ERR_INVALID_ARG  # causal needs Lq == Lk
+    m2 = binding.MaskT(); m2.dense = 4096; m2.dense_mq = 3
+    assert _call_forward(lib, mask=m2) == binding.MHA_ERR_INVALID_ARG             # dense_mq not 1 / Lq
+    assert _call_forward(lib, ws=16) == binding.MHA_ERR_INVALID_ARG               # workspace too small
+    assert _call_forward(lib, ws_ptr=260) == binding.MHA_ERR_INVALID_ARG          # misaligned workspace
+    assert _call_forward(lib, ptr=4097) == binding.MHA_ERR_INVALID_ARG            # misaligned bf16 tensor
+    P = ctypes.c_void_p(4096)
+    rc = lib.mha_forward(binding.MHA_BF16, None, P, P, P, None, P, None, P, None, P, None, 1, 4, 4, 128, 2,
+                         None, P, None, ctypes.c_void_p(256), 1 << 30, None)
+    assert rc == binding.MHA_ERR_INVALID_ARG                                       # null query
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(ImportError):
+        binding._lib = None
+        try:
+            binding.load(str(tmp_path / "missing.so"))
+        finally:
+            binding._lib = None

@@ -1,0 +1,232 @@
+"""GPU path vs the fp64 oracle, element by element, through the C ABI.
+
+Inputs are seeded and bf16-rounded before both paths (workloads module).
+Tolerances: bf16 |g-o| <= 1.5e-2 + 2e-2|o|; fp32 |g-o| <= 1e-4 + 1e-4|o|;
+p_attn rows sum to 1 within 1e-3.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from transformer_head_scaled_fwd_gb300 import workloads as W  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from transformer_head_scaled_fwd_gb300 import build as B
+    B.build()
+    from transformer_head_scaled_fwd_gb300 import binding
+    binding.load()
+    binding.mha_check_device_status(reset=True)
+
+
+from gpu_helpers import ROWSUM_TOL, assert_close, run_gpu, run_oracle  # noqa: E402
+
+
+def _worked_example_inputs(dtype):
+    g = json.load(open(os.path.join(GOLDEN, "thinking_machines.json")))
+    d = g["d_k"]
+    wl = W.Workload("worked", 0, dtype, 1, 1, 2, d, 1, False, False)
+    eye = np.eye(d, dtype=np.float32)
+    q = np.zeros((1, 1, d), np.float32); q[0, 0, 0] = 1
+    k = np.zeros((1, 2, d), np.float32); k[0, 0, 0] = g["raw_scores"][0]; k[0, 1, 0] = g["raw_scores"][1]
+    v = np.zeros((1, 2, d), np.float32); v[0, 0, 0] = 1; v[0, 1, 1] = 1
+    w = {"w_q": eye, "w_k": eye, "w_v": eye, "w_o": eye}
+    for n in "qkvo":
+        w["b_" + n] = np.zeros(d, np.float32)
+    return W.Inputs(wl, q, k, v, w), g
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_worked_example_thinking_machines(dtype):
+    inp, g = _worked_example_inputs(dtype)
+    out, p = run_gpu(inp, want_p_attn=True)
+    tol = 1e-6 if dtype == "f32" else 5e-3
+    np.testing.assert_allclose(p[0, 0, 0], g["weights"], rtol=0, atol=tol)
+    expect = np.zeros(inp.wl.d_model); expect[:2] = g["weights"]
+    np.testing.assert_allclose(out[0, 0], expect, rtol=0, atol=tol if dtype == "f32" else 1e-2)
+
+
+def test_tiny_fp32_config_with_p_attn():
+    inp = W.make_inputs(W.WORKLOADS["tiny"])
+    got, gp = run_gpu(inp, valid_lens=inp.valid_lens, want_p_attn=True)
+    ref, rp = run_oracle(inp, valid_lens=inp.valid_lens, want_p_attn=True)
+    assert_close(got, ref, "f32")
+    assert_close(gp, rp, "f32", "p_attn")
+    np.testing.assert_allclose(gp.sum(-1), 1.0, atol=ROWSUM_TOL)
+
+
+@pytest.mark.parametrize("name", ["enc", "dec", "xattn"])
+def test_bf16_configs_full(name):
+    wl = W.WORKLOADS[name]
+    inp = W.make_inputs(wl)
+    got, _ = run_gpu(inp, causal=wl.causal, valid_lens=inp.valid_lens)
+    ref = run_oracle(inp, causal=wl.causal, valid_lens=inp.valid_lens)
+    assert_close(got, ref, "bf16")
+
+
+def test_long_causal_sampled_rows():
+    wl = W.WORKLOADS["long"]
+    inp = W.make_inputs(wl)
+    rows = W.sample_rows(wl.Lq, 64, seed=4)
+    got, _ = run_gpu(inp, causal=True)
+    ref = run_oracle(inp, causal=True, rows=rows)
+    assert_close(got[:, rows], ref, "bf16")
+
+
+# ------------------------------------------------------------------ edge cases (bf16)
+def test_ragged_cross_attention_distinct_kv_bias_p_attn():
+    inp = W.random_case(1, 3, 200, 77, 512, 8, kv_alias=False, bias_scale=0.1)
+    vl = [77, 1, 40]
+    got, gp = run_gpu(inp, valid_lens=vl, want_p_attn=True)
+    ref, rp = run_oracle(inp, valid_lens=vl, want_p_attn=True)
+    assert_close(got, ref, "bf16")
+    assert_close(gp, rp, "bf16", "p_attn")
+    np.testing.assert_allclose(gp.sum(-1), 1.0, atol=ROWSUM_TOL)
+    assert np.all(gp[1, :, :, 1:] == 0.0)
+
+
+@pytest.mark.parametrize("L", [1, 2, 3, 10, 129, 300])
+def test_causal_self_attention_small_and_ragged(L):
+    inp = W.random_case(10 + L, 2, L, L, 256, 4, self_attn=True)
+    vl = [L, max(1, L // 2)]
+    got, gp = run_gpu(inp, causal=True, valid_lens=vl, want_p_attn=L <= 300)
+    ref, rp = run_oracle(inp, causal=True, valid_lens=vl, want_p_attn=True)
+    assert_close(got, ref, "bf16")
+    assert_close(gp, rp, "bf16", "p_attn")
+
+
+def test_fully_masked_rows_are_uniform():
+    """valid length 0: every score is -1e9, weights 1/L_k over all keys."""
+    inp = W.random_case(30, 3, 70, 150, 256, 4)
+    vl = [0, 150, 3]
+    got, gp = run_gpu(inp, valid_lens=vl, want_p_attn=True)
+    ref, rp = run_oracle(inp, valid_lens=vl, want_p_attn=True)
+    assert_close(got, ref, "bf16")
+    np.testing.assert_allclose(gp[0], 1.0 / 150, rtol=1e-5, atol=0)
+    assert_close(gp, rp, "bf16", "p_attn")
+
+
+@pytest.mark.parametrize("mq", ["broadcast", "per_query"])
+def test_dense_mask(mq):
+    B, Lq, Lk = 2, 140, 260
+    inp = W.random_case(40, B, Lq, Lk, 256, 4)
+    rng = np.random.default_rng(41)
+    dense = (rng.random((B, 1 if mq == "broadcast" else Lq, Lk)) < 0.7).astype(np.uint8)
+    dense[1, 0, :] = 0                         # a fully masked row (all rows if broadcast)
+    got, gp = run_gpu(inp, dense=dense, want_p_attn=True)
+    ref, rp = run_oracle(inp, dense=dense, want_p_attn=True)
+    assert_close(got, ref, "bf16")
+    assert_close(gp, rp, "bf16", "p_attn")
+
+
+def test_dense_mask_with_causal_and_padding():
+    B, L = 2, 260
+    inp = W.random_case(42, B, L, L, 256, 4, self_attn=True)
+    rng = np.random.default_rng(43)
+    dense = (rng.random((B, L, L)) < 0.8).astype(np.uint8)
+    vl = [200, 0]
+    got, _ = run_gpu(inp, causal=True, valid_lens=vl, dense=dense)
+    ref = run_oracle(inp, causal=True, valid_lens=vl, dense=dense)
+    assert_close(got, ref, "bf16")
+
+
+@pytest.mark.parametrize("h", [1, 3])
+def test_odd_head_counts(h):
+    d = 64 * h
+    inp = W.random_case(50 + h, 2, 150, 131, d, h, bias_scale=0.2)
+    got, _ = run_gpu(inp, valid_lens=[131, 60])
+    ref = run_oracle(inp, valid_lens=[131, 60])
+    assert_close(got, ref, "bf16")
+
+
+def test_stage_entry_points_equal_forward():
+    inp = W.random_case(60, 2, 256, 256, 512, 8, self_attn=True)
+    a, _ = run_gpu(inp, causal=True)
+    b, _ = run_gpu(inp, causal=True, stages=True)
+    np.testing.assert_array_equal(a, b)
+
+
+def test_masked_keys_do_not_change_output():
+    inp = W.random_case(70, 2, 130, 300, 256, 4)
+    vl = [300, 150]
+    a, _ = run_gpu(inp, valid_lens=vl)
+    inp.key = inp.key.copy(); inp.value = inp.key
+    inp.key[1, 150:] = np.float32(7.0) * np.sign(inp.key[1, 150:])
+    b, _ = run_gpu(inp, valid_lens=vl)
+    np.testing.assert_array_equal(a, b)
+
+
+def test_identical_query_rows_identical_outputs():
+    inp = W.random_case(80, 1, 300, 200, 256, 4)
+    inp.query = inp.query.copy()
+    inp.query[0, 257] = inp.query[0, 3]
+    out, _ = run_gpu(inp)
+    np.testing.assert_array_equal(out[0, 257], out[0, 3])
+
+
+# ------------------------------------------------------------------ fp32 path
+@pytest.mark.parametrize("d,h", [(512, 16), (512, 4), (32, 4), (96, 1)])
+def test_fp32_head_widths(d, h):
+    inp = W.random_case(90 + h, 2, 37, 45, d, h, dtype="f32")
+    vl = [45, 0]
+    got, gp = run_gpu(inp, valid_lens=vl, want_p_attn=True)
+    ref, rp = run_oracle(inp, valid_lens=vl, want_p_attn=True)
+    assert_close(got, ref, "f32")
+    assert_close(gp, rp, "f32", "p_attn")
+
+
+def test_fp32_causal_dense():
+    inp = W.random_case(99, 2, 33, 33, 128, 2, dtype="f32", self_attn=True)
+    dense = (np.random.default_rng(5).random((2, 33, 33)) < 0.6).astype(np.uint8)
+    got, _ = run_gpu(inp, causal=True, dense=dense)
+    ref = run_oracle(inp, causal=True, dense=dense)
+    assert_close(got, ref, "f32")
+
+
+# ------------------------------------------------------------------ host-buffer entry point
+def test_forward_host_matches_device_path():
+    from transformer_head_scaled_fwd_gb300 import binding
+    from gpu_helpers import to_dev
+    inp = W.random_case(100, 2, 192, 192, 512, 8, self_attn=True)
+    dev_out, _ = run_gpu(inp, causal=True)
+    dt = torch.bfloat16
+    hq = torch.from_numpy(inp.query).to(dt).pin_memory()
+    hout = torch.empty_like(hq).pin_memory()
+    Wd = {n: to_dev(a, dt) for n, a in inp.weights.items()}
+    B, L, d = inp.query.shape
+    staging = torch.empty(binding.host_staging_size(binding.MHA_BF16, B, L, L, d, False, False),
+                          dtype=torch.uint8, device="cuda")
+    ws = torch.empty(binding.workspace_size(binding.MHA_BF16, B, L, L, d, 8), dtype=torch.uint8, device="cuda")
+    binding.mha_forward_host(hq, hq, hq, Wd["w_q"], Wd["b_q"], Wd["w_k"], Wd["b_k"], Wd["w_v"], Wd["b_v"],
+                             Wd["w_o"], Wd["b_o"], 8, h_out=hout, staging=staging, workspace=ws,
+                             mask=binding.make_mask(causal=True))
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(hout.double().numpy(), dev_out)
+
+
+def test_invalid_arguments_leave_output_untouched():
+    from transformer_head_scaled_fwd_gb300 import binding
+    dt = torch.bfloat16
+    x = torch.zeros(1, 8, 96, dtype=dt, device="cuda")
+    w = torch.zeros(96, 96, dtype=dt, device="cuda")
+    out = torch.full((1, 8, 96), 3.0, dtype=dt, device="cuda")
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    with pytest.raises(binding.MHAError) as e:
+        binding.mha_forward(x, x, x, w, None, w, None, w, None, w, None, 5, out=out, workspace=ws)
+    assert e.value.status == binding.MHA_ERR_INVALID_ARG
+    with pytest.raises(binding.MHAError) as e:       # d_k = 48 on the bf16 path
+        binding.mha_forward(x, x, x, w, None, w, None, w, None, w, None, 2, out=out, workspace=ws)
+    assert e.value.status == binding.MHA_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert torch.all(out == 3.0)

@@ -1,0 +1,436 @@
+// attn_tc.cu -- fused scaled dot-product attention on the 5th-generation tensor cores.
+//
+// Per (batch, head) it computes "The Annotated Transformer", section
+// "Attention", attention():
+//     scores = Q K^T / sqrt(d_k);  scores.masked_fill(mask == 0, -1e9);
+//     p_attn = softmax(scores, dim=-1);  head = p_attn V
+// and writes the head's output into its d_k-wide column slab of the
+// concatenated context [B, L_q, h*d_k] ("003-Transformer" tutorial,
+// MultiHeadedAttention.forward: transpose(1, 2).contiguous().view(B, -1, h*d_k)),
+// so the concat is a strided TMA store and no transpose kernel runs.
+//
+// The softmax is taken online over key tiles (running row max m and row sum l,
+// the accumulated output rescaled when m grows), which is an exact rewrite of
+// softmax-then-matmul: the L_q x L_k score matrix never leaves the chip.
+//
+// CTA = two 128-row query tiles (t = 0, 1) of one (batch, head); key tiles of 128.
+// Tensor memory (512 columns): S_t at columns [128t, 128t+128) (fp32 scores),
+// P_t (bf16 weights, two per column) overwrites the first 64 columns of S_t,
+// O_t (fp32 output accumulator) at columns [256 + 64t, 256 + 64t + 64).
+// Warp roles:
+//   warps 0-3 / 4-7   softmax for query tile 0 / 1: one thread per query row.
+//                     tcgen05.ld the score row, scale to log2 units, apply the
+//                     -1e9 fill, update (m, l), rescale O when m grows by more
+//                     than 2^8 (lazy: exact, the final O / l uses the same m),
+//                     write P into tensor memory with tcgen05.st.
+//   warp 8            TMA: Q tiles once, K and V tiles through a 3-deep ring.
+//   warp 9            allocates tensor memory; tcgen05.mma from one thread: S_t = Q_t K^T (SS, M=128,
+//                     N=128), O_t += P_t V (A from tensor memory, V MN-major,
+//                     M=128, N=64), interleaved so one tile's softmax overlaps
+//                     the other tile's MMAs.
+//   warps 10-11       idle (they complete the third warpgroup).
+// Registers: launched at 168 per thread (384 threads); the third warpgroup
+// drops to 56 and the two softmax warpgroups rise to 224
+// (128*56 + 256*224 = 64512 = 384*168, the launch total).
+#include <math_constants.h>
+
+#include "mha_internal.h"
+#include "ptx.cuh"
+
+namespace mha {
+namespace {
+
+constexpr uint32_t kTileBytes = 128 * 128;          // 128 rows x 64 bf16 = 16 KB
+constexpr uint32_t kTmemCols = 512;
+constexpr float kMaskedLog2 = -1.0e9f * 1.4426950408889634f;   // the -1e9 fill, in log2 units
+constexpr float kRescaleThreshold = 8.0f;           // lazy rescale: only when m grows by > 2^8
+
+struct AttnSmem {
+    uint64_t q_full;
+    uint64_t k_full[kAttnStages];
+    uint64_t v_full[kAttnStages];
+    uint64_t k_empty[kAttnStages];
+    uint64_t v_empty[kAttnStages];
+    uint64_t s_full[2];
+    uint64_t p_full[2];
+    uint64_t o_full[2];
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+// [Q0 | Q1 | K ring | V ring | AttnSmem], tiles 1024-aligned.
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffK = 2 * kTileBytes;
+constexpr uint32_t kOffV = kOffK + kAttnStages * kTileBytes;
+constexpr uint32_t kOffBar = kOffV + kAttnStages * kTileBytes;
+constexpr size_t kSmemBytes = 1024 + kOffBar + sizeof(AttnSmem);
+
+struct TileWork {
+    int n;          // key tiles this query tile processes
+    bool active;    // query tile has rows < L_q
+};
+
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __grid_constant__ AttnParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    AttnSmem* sm = reinterpret_cast<AttnSmem*>(base + kOffBar);
+
+    // Longest-first order: blocks are dispatched in index order, and with the
+    // causal mask the last query tiles carry the most key tiles.
+    const int BH = p.B * p.h;
+    const int qp = p.q_pairs - 1 - static_cast<int>(blockIdx.x) / BH;
+    const int bh = static_cast<int>(blockIdx.x) % BH;
+    const int b = bh / p.h;
+    const int head = bh - b * p.h;
+    const int q0 = qp * 2 * kAttnBM;
+
+    // Key range. With at least one allowed key per row (valid length >= 1 and
+    // no dense mask), key tiles that are fully masked for every row of a query
+    // tile add exactly zero and are skipped. Otherwise every key is visited, so
+    // that a fully masked row comes out uniform over all L_k keys.
+    int vl = p.Lk;
+    if (p.valid_lens != nullptr) vl = min(max(p.valid_lens[b], 0), p.Lk);
+    const bool can_skip = (p.dense == nullptr) && (vl >= 1);
+    TileWork tw[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int qt0 = q0 + t * kAttnBM;
+        tw[t].active = qt0 < p.Lq;
+        int kend = can_skip ? vl : p.Lk;
+        if (can_skip && p.causal) kend = min(kend, qt0 + kAttnBM);
+        tw[t].n = tw[t].active ? (kend + kAttnBN - 1) / kAttnBN : 0;
+    }
+    const int n_all = max(tw[0].n, tw[1].n);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int q_slab = b * p.h + head;
+    const int k_slab = b * 2 * p.h + head;
+    const int v_slab = k_slab + p.h;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&sm->q_full, 1);
+        for (int s = 0; s < kAttnStages; ++s) {
+            mbar_init(&sm->k_full[s], 1);
+            mbar_init(&sm->v_full[s], 1);
+            mbar_init(&sm->k_empty[s], 1);
+            mbar_init(&sm->v_empty[s], 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&sm->s_full[t], 1);
+            mbar_init(&sm->p_full[t], kAttnBM);
+            mbar_init(&sm->o_full[t], 1);
+        }
+        sm->abort_flag = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&p.q_map);
+        tma_prefetch_desc(&p.kv_map);
+        tma_prefetch_desc(&p.ctx_map);
+    }
+    if (warp == 9) {
+        tmem_alloc(&sm->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm->tmem_base;
+    volatile int* abort_flag = &sm->abort_flag;
+
+    // The two register-budget regions never rejoin: each ends with its own
+    // copy of the teardown barrier (id 3, all 384 threads).
+    if (warp >= 8) {
+      regs_dec<56>();
+      if (warp == 8) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t qbytes = (tw[0].n > 0 ? kTileBytes : 0) + (tw[1].n > 0 ? kTileBytes : 0);
+            mbar_arrive_expect_tx(&sm->q_full, qbytes);
+            if (tw[0].n > 0) tma_load_3d(&p.q_map, &sm->q_full, base + kOffQ, 0, q0, q_slab);
+            if (tw[1].n > 0) tma_load_3d(&p.q_map, &sm->q_full, base + kOffQ + kTileBytes, 0, q0 + kAttnBM, q_slab);
+            for (int j = 0; j < n_all; ++j) {
+                const int s = j % kAttnStages;
+                const uint32_t ph = (j / kAttnStages) & 1;
+                mbar_wait(&sm->k_empty[s], ph ^ 1, abort_flag, p.status, 0x201);
+                mbar_arrive_expect_tx(&sm->k_full[s], kTileBytes);
+                tma_load_3d(&p.kv_map, &sm->k_full[s], base + kOffK + s * kTileBytes, 0, j * kAttnBN, k_slab);
+                mbar_wait(&sm->v_empty[s], ph ^ 1, abort_flag, p.status, 0x202);
+                mbar_arrive_expect_tx(&sm->v_full[s], kTileBytes);
+                tma_load_3d(&p.kv_map, &sm->v_full[s], base + kOffV + s * kTileBytes, 0, j * kAttnBN, v_slab);
+            }
+        }
+    } else if (warp == 9) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0 && n_all > 0) {
+            constexpr uint32_t idesc_s = idesc_bf16(kAttnBM, kAttnBN, false, false);
+            constexpr uint32_t idesc_o = idesc_bf16(kAttnBM, kAttnD, false, true);
+            const uint32_t q_addr = smem_u32(base + kOffQ);
+            const uint32_t k_addr = smem_u32(base + kOffK);
+            const uint32_t v_addr = smem_u32(base + kOffV);
+            auto issue_s = [&](int t, int s) {
+                const uint32_t qa = q_addr + t * kTileBytes;
+                const uint32_t ka = k_addr + s * kTileBytes;
+#pragma unroll
+                for (int k = 0; k < kAttnD / 16; ++k)
+                    mma_ss(tmem + t * 128, sdesc_sw128(qa + k * 32, 16, 1024), sdesc_sw128(ka + k * 32, 16, 1024),
+                           idesc_s, k > 0);
+                tc_commit(&sm->s_full[t]);
+            };
+            auto issue_pv = [&](int t, int s, bool acc) {
+                const uint32_t va = v_addr + s * kTileBytes;
+#pragma unroll
+                for (int k = 0; k < kAttnBN / 16; ++k)
+                    mma_ts(tmem + 256 + t * 64, tmem + t * 128 + k * 8, sdesc_sw128(va + k * 2048, 8192, 1024),
+                           idesc_o, (acc || k > 0) ? 1u : 0u);
+            };
+            mbar_wait(&sm->q_full, 0, abort_flag, p.status, 0x203);
+            mbar_wait(&sm->k_full[0], 0, abort_flag, p.status, 0x204);
+            tc_fence_after();
+            if (tw[0].n > 0) issue_s(0, 0);
+            if (tw[1].n > 0) issue_s(1, 0);
+            tc_commit(&sm->k_empty[0]);
+            for (int j = 0; j < n_all; ++j) {
+                const int s = j % kAttnStages;
+                const uint32_t ph = (j / kAttnStages) & 1;
+                const bool has_next = j + 1 < n_all;
+                const int s1 = (j + 1) % kAttnStages;
+                const uint32_t ph1 = ((j + 1) / kAttnStages) & 1;
+                mbar_wait(&sm->v_full[s], ph, abort_flag, p.status, 0x205);
+                if (has_next) mbar_wait(&sm->k_full[s1], ph1, abort_flag, p.status, 0x206);
+                tc_fence_after();
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    if (j < tw[t].n) {
+                        mbar_wait(&sm->p_full[t], j & 1, abort_flag, p.status, 0x207);
+                        tc_fence_after();
+                        issue_pv(t, s, j > 0);
+                        if (j == tw[t].n - 1) tc_commit(&sm->o_full[t]);
+                    }
+                    if (j + 1 < tw[t].n) issue_s(t, s1);
+                }
+                tc_commit(&sm->v_empty[s]);
+                if (has_next) tc_commit(&sm->k_empty[s1]);
+            }
+        }
+    }
+    tc_fence_before();
+    named_bar_sync(3, kAttnThreads);
+    if (warp == 9) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+    } else {
+        regs_inc<224>();
+        // ------------------------------------------------ softmax, one thread per query row
+        const int t = warp >> 2;
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const int qt0 = q0 + t * kAttnBM;
+        const int qi = qt0 + row;
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t s_tmem = tmem + lane_off + t * 128;
+        const uint32_t o_tmem = tmem + lane_off + 256 + t * 64;
+        const int n = tw[t].n;
+        float m = -CUDART_INF_F;
+        float l = 0.0f;
+
+        for (int j = 0; j < n; ++j) {
+            mbar_wait(&sm->s_full[t], j & 1, abort_flag, p.status, 0x208);
+            __syncwarp();
+            tc_fence_after();
+            uint32_t u[128];   // raw fp32 scores of this row
+            tmem_ld_x64(s_tmem, *reinterpret_cast<uint32_t(*)[64]>(&u[0]));
+            tmem_ld_x64(s_tmem + 64, *reinterpret_cast<uint32_t(*)[64]>(&u[64]));
+            const int k0 = j * kAttnBN;
+            const bool edge = (p.dense != nullptr) || (k0 + kAttnBN > vl) ||
+                              (p.causal && k0 + kAttnBN - 1 > qt0);
+            // Full tiles keep raw scores and fold the scale into the exponent
+            // (scale > 0, so max commutes with it); edge tiles are rewritten in
+            // log2 units with the fill applied, and use scale 1.
+            float sc = p.scale_log2;
+            if (edge) {
+                // keys c < lim pass the causal and valid-length parts; c >= oob are past L_k
+                const int lim = min(vl, p.causal ? qi + 1 : p.Lk) - k0;
+                const int oob = p.Lk - k0;
+#pragma unroll
+                for (int c = 0; c < 128; ++c) {
+                    const float x = (c < lim) ? __uint_as_float(u[c]) * sc : kMaskedLog2;   // -1e9 fill, after scaling
+                    u[c] = __float_as_uint((c < oob) ? x : -CUDART_INF_F);                   // not a key at all
+                }
+                if (p.dense != nullptr && qi < p.Lq) {
+                    const long mrow = (p.dense_mq == 1) ? 0 : qi;
+                    const long mq = (p.dense_mq == 1) ? 1 : p.Lq;
+                    const uint8_t* mr = p.dense + (static_cast<long>(b) * mq + mrow) * p.Lk + k0;
+                    uint32_t keep[4];   // bit c: dense mask allows key k0 + c
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        uint32_t bits = 0;
+#pragma unroll 1
+                        for (int c = 0; c < 32; ++c)
+                            if (32 * w + c >= oob || mr[32 * w + c] != 0) bits |= 1u << c;
+                        keep[w] = bits;
+                    }
+#pragma unroll
+                    for (int c = 0; c < 128; ++c)
+                        if (!((keep[c >> 5] >> (c & 31)) & 1u)) u[c] = __float_as_uint(kMaskedLog2);
+                }
+                sc = 1.0f;
+            }
+            float mt = __uint_as_float(u[0]);
+#pragma unroll
+            for (int c = 1; c < 128; ++c) mt = fmaxf(mt, __uint_as_float(u[c]));
+            const float m_new = fmaxf(m, mt * sc);
+            if (j == 0) {
+                m = m_new;
+            } else {
+                const bool grow = (m_new - m) > kRescaleThreshold;
+                if (__any_sync(0xffffffffu, grow)) {
+                    const float alpha = grow ? ex2_approx(m - m_new) : 1.0f;
+                    if (grow) {
+                        l *= alpha;
+                        m = m_new;
+                    }
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint32_t o[16];
+                        tmem_ld_x16(o_tmem + q4 * 16, o);
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                        tmem_st_x16(o_tmem + q4 * 16, o);
+                    }
+                }
+            }
+            const float neg_m = -m;
+            float lsum = 0.0f;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const float p0 = ex2_approx(fmaf(__uint_as_float(u[32 * q4 + 2 * c]), sc, neg_m));
+                    const float p1 = ex2_approx(fmaf(__uint_as_float(u[32 * q4 + 2 * c + 1]), sc, neg_m));
+                    lsum += p0 + p1;
+                    pk[c] = pack_bf16x2(p0, p1);
+                }
+                tmem_st_x16(s_tmem + q4 * 16, pk);
+            }
+            l += lsum;
+            tc_fence_before();
+            mbar_arrive(&sm->p_full[t]);
+        }
+
+        // ---------------- epilogue: O / l -> bf16 -> the head's slab of ctx
+        if (n > 0) {
+            mbar_wait(&sm->o_full[t], 0, abort_flag, p.status, 0x209);
+            __syncwarp();
+            tc_fence_after();
+            uint32_t o[64];
+            tmem_ld_x64(o_tmem, o);
+            const float inv = 1.0f / l;
+            // Q_t's tile is free (its last MMA completed before o_full): stage there.
+            const uint32_t stage = smem_u32(base + kOffQ + t * kTileBytes) + row * 128;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    w[e] = pack_bf16x2(__uint_as_float(o[ch * 8 + 2 * e]) * inv,
+                                       __uint_as_float(o[ch * 8 + 2 * e + 1]) * inv);
+                st_shared_v4(stage + ((ch ^ (row & 7)) << 4), w[0], w[1], w[2], w[3]);
+            }
+            if (p.stats != nullptr && qi < p.Lq) {
+                float2* st = reinterpret_cast<float2*>(p.stats) + (static_cast<long>(q_slab) * p.Lq + qi);
+                *st = make_float2(m, l);
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(1 + t, kAttnBM);
+            if (row == 0 && !*abort_flag) {
+                tma_store_3d(&p.ctx_map, base + kOffQ + t * kTileBytes, head * kAttnD, qt0, b);
+                tma_store_commit();
+                tma_store_wait_all();
+            }
+        }
+        tc_fence_before();
+        named_bar_sync(3, kAttnThreads);
+    }
+}
+
+// ------------------------------------------------------------------ p_attn (bf16 path)
+// p_attn[b, h, i, j] = exp2(u_ij - m_i) / l_i with the row statistics written by
+// the attention kernel; u_ij recomputed from the bf16 Qh, Kh in fp32.
+constexpr int kPRows = 32;     // query rows per block
+constexpr int kPKeys = 128;    // keys per pass (one per thread)
+
+__global__ void __launch_bounds__(kPKeys) pattn_bf16_kernel(const PattnParams p) {
+    __shared__ float qs[kPRows][kAttnD];
+    __shared__ float2 st[kPRows];
+    const int bh = blockIdx.y;
+    const int b = bh / p.h;
+    const int head = bh - b * p.h;
+    const int i0 = blockIdx.x * kPRows;
+    const __nv_bfloat16* q = p.q + (static_cast<long>(bh) * p.Lq) * kAttnD;
+    const __nv_bfloat16* k = p.kv + (static_cast<long>(b) * 2 * p.h + head) * p.Lk * kAttnD;
+    for (int e = threadIdx.x; e < kPRows * kAttnD; e += blockDim.x) {
+        const int r = e / kAttnD, c = e % kAttnD;
+        qs[r][c] = (i0 + r < p.Lq) ? __bfloat162float(q[static_cast<long>(i0 + r) * kAttnD + c]) : 0.0f;
+    }
+    for (int r = threadIdx.x; r < kPRows; r += blockDim.x)
+        st[r] = (i0 + r < p.Lq) ? reinterpret_cast<const float2*>(p.stats)[static_cast<long>(bh) * p.Lq + i0 + r]
+                                : make_float2(0.f, 1.f);
+    __syncthreads();
+    int vl = p.Lk;
+    if (p.valid_lens != nullptr) vl = min(max(p.valid_lens[b], 0), p.Lk);
+    for (int k0 = 0; k0 < p.Lk; k0 += kPKeys) {
+        const int kj = k0 + threadIdx.x;
+        if (kj >= p.Lk) continue;
+        float kr[kAttnD];
+#pragma unroll
+        for (int c = 0; c < kAttnD; c += 8) {
+            const uint4 raw = *reinterpret_cast<const uint4*>(k + static_cast<long>(kj) * kAttnD + c);
+            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __bfloat1622float2(h2[e]);
+                kr[c + 2 * e] = f.x;
+                kr[c + 2 * e + 1] = f.y;
+            }
+        }
+        for (int r = 0; r < kPRows; ++r) {
+            const int qi = i0 + r;
+            if (qi >= p.Lq) break;
+            float dot = 0.f;
+#pragma unroll
+            for (int c = 0; c < kAttnD; ++c) dot = fmaf(qs[r][c], kr[c], dot);
+            bool ok = !(p.causal && kj > qi) && kj < vl;
+            if (ok && p.dense != nullptr) {
+                const long mrow = (p.dense_mq == 1) ? 0 : qi;
+                const long mq = (p.dense_mq == 1) ? 1 : p.Lq;
+                ok = p.dense[(static_cast<long>(b) * mq + mrow) * p.Lk + kj] != 0;
+            }
+            const float u = ok ? dot * p.scale_log2 : kMaskedLog2;
+            p.p_attn[(static_cast<long>(bh) * p.Lq + qi) * p.Lk + kj] = ex2_approx(u - st[r].x) / st[r].y;
+        }
+    }
+}
+
+}  // namespace
+
+size_t attn_tc_smem_bytes() { return kSmemBytes; }
+
+cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t s) {
+    cudaError_t e = cudaFuncSetAttribute(attn_bf16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    const unsigned grid = static_cast<unsigned>(p.q_pairs) * p.B * p.h;
+    attn_bf16_tc_kernel<<<grid, kAttnThreads, kSmemBytes, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pattn_bf16(const PattnParams& p, cudaStream_t s) {
+    dim3 grid((p.Lq + kPRows - 1) / kPRows, p.B * p.h);
+    pattn_bf16_kernel<<<grid, kPKeys, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace mha

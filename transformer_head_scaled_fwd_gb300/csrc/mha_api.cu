@@ -1,0 +1,478 @@
+// mha_api.cu -- the C ABI declared in include/mha.h: argument validation,
+// workspace layout, TMA tensor-map encoding and the three-stage dispatch of
+// MultiHeadedAttention.forward ("003-Transformer" tutorial, section
+// "Multi-head attention"): projections + head split, attention per head +
+// concat, output projection.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "../../include/mha.h"
+#include "mha_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+__device__ int g_device_status;   // bounded-wait give-ups recorded by the kernels
+
+mha_status_t fail(mha_status_t st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+mha_status_t cuda_fail(cudaError_t e, const char* what) {
+    return fail(MHA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// ---------------------------------------------------------------- workspace layout
+struct Layout {
+    size_t q, kv, ctx, stat, total;
+};
+
+bool layout_of(mha_dtype_t dt, int B, int Lq, int Lk, int d, int h, Layout* L) {
+    if (B <= 0 || Lq <= 0 || Lk <= 0 || d <= 0 || h <= 0 || d % h != 0) return false;
+    if (dt != MHA_F32 && dt != MHA_BF16) return false;
+    const size_t es = dt == MHA_BF16 ? 2 : 4;
+    const size_t dk = static_cast<size_t>(d / h);
+    L->q = 0;
+    L->kv = align256(L->q + es * B * h * static_cast<size_t>(Lq) * dk);
+    L->ctx = align256(L->kv + es * B * 2 * h * static_cast<size_t>(Lk) * dk);
+    L->stat = align256(L->ctx + es * B * static_cast<size_t>(Lq) * d);
+    L->total = align256(L->stat + sizeof(float) * 2 * B * h * static_cast<size_t>(Lq));
+    return true;
+}
+
+// ---------------------------------------------------------------- tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+mha_status_t get_encoder() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (g_encode == nullptr) return fail(MHA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    return MHA_OK;
+}
+
+// bf16 tiled map, 128-byte swizzle, zero fill out of bounds.
+mha_status_t encode_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                         const uint64_t* strides_bytes, const uint32_t* box, const char* what) {
+    uint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides_bytes,
+                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MHA_ERR_CUDA, "tensor map encode failed for %s (CUresult %d)", what, (int)r);
+    return MHA_OK;
+}
+
+// [B, L, N] row-major bf16 as {N, L, B}, box {64, 128, 1}
+mha_status_t map_rows(CUtensorMap* m, const void* base, int B, int L, int N, const char* what) {
+    const uint64_t dims[3] = {(uint64_t)N, (uint64_t)L, (uint64_t)B};
+    const uint64_t str[2] = {(uint64_t)N * 2, (uint64_t)L * N * 2};
+    const uint32_t box[3] = {64, 128, 1};
+    return encode_bf16(m, base, 3, dims, str, box, what);
+}
+// weight [N, K] as {K, N}, box {64, 128}
+mha_status_t map_weight(CUtensorMap* m, const void* base, int N, int K) {
+    const uint64_t dims[2] = {(uint64_t)K, (uint64_t)N};
+    const uint64_t str[1] = {(uint64_t)K * 2};
+    const uint32_t box[2] = {64, 128};
+    return encode_bf16(m, base, 2, dims, str, box, "weight");
+}
+// head-split [B, slabs, L, 64] as {64, L, slabs, B}, box {64, 128, 1, 1}
+mha_status_t map_heads4(CUtensorMap* m, const void* base, int B, int slabs, int L) {
+    const uint64_t dims[4] = {64, (uint64_t)L, (uint64_t)slabs, (uint64_t)B};
+    const uint64_t str[3] = {128, (uint64_t)L * 128, (uint64_t)slabs * L * 128};
+    const uint32_t box[4] = {64, 128, 1, 1};
+    return encode_bf16(m, base, 4, dims, str, box, "head-split output");
+}
+// head-split [planes, L, 64] as {64, L, planes}, box {64, 128, 1}
+mha_status_t map_heads3(CUtensorMap* m, const void* base, int planes, int L) {
+    const uint64_t dims[3] = {64, (uint64_t)L, (uint64_t)planes};
+    const uint64_t str[2] = {128, (uint64_t)L * 128};
+    const uint32_t box[3] = {64, 128, 1};
+    return encode_bf16(m, base, 3, dims, str, box, "head-split input");
+}
+
+int* device_status_ptr() {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+    return static_cast<int*>(p);
+}
+
+// ---------------------------------------------------------------- validation
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+mha_status_t check_sizes(mha_dtype_t dt, int B, int Lq, int Lk, int d, int h) {
+    if (dt != MHA_F32 && dt != MHA_BF16) return fail(MHA_ERR_INVALID_ARG, "dtype %d is not MHA_F32 or MHA_BF16", dt);
+    if (B <= 0 || Lq <= 0 || Lk <= 0 || d <= 0 || h <= 0)
+        return fail(MHA_ERR_INVALID_ARG, "sizes must be positive (B=%d L_q=%d L_k=%d d_model=%d h=%d)", B, Lq, Lk, d,
+                    h);
+    if (d % h != 0) return fail(MHA_ERR_INVALID_ARG, "d_model %% h != 0 (d_model=%d, h=%d)", d, h);
+    const int dk = d / h;
+    if (dt == MHA_BF16 && dk != 64)
+        return fail(MHA_ERR_UNSUPPORTED, "bf16 path implements d_k = 64 only (d_k = %d)", dk);
+    if (dt == MHA_F32 && dk > 256) return fail(MHA_ERR_UNSUPPORTED, "fp32 path implements d_k <= 256 (d_k = %d)", dk);
+    const double big = static_cast<double>(B) * h * Lq * Lk;
+    if (static_cast<double>(B) * Lq * d > 4.0e9 || static_cast<double>(B) * Lk * d * 2 > 4.0e9 || big > 1.0e15)
+        return fail(MHA_ERR_UNSUPPORTED, "problem too large for 32-bit tile indices");
+    return MHA_OK;
+}
+
+mha_status_t check_workspace(mha_dtype_t dt, int B, int Lq, int Lk, int d, int h, const void* ws, size_t bytes,
+                             Layout* L) {
+    layout_of(dt, B, Lq, Lk, d, h, L);
+    if (ws == nullptr) return fail(MHA_ERR_INVALID_ARG, "workspace is NULL");
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(MHA_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+    if (bytes < L->total)
+        return fail(MHA_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", bytes, L->total);
+    return MHA_OK;
+}
+
+mha_status_t check_mask(const mha_mask_t* mask, int Lq, int Lk) {
+    if (mask == nullptr) return MHA_OK;
+    if (mask->causal && Lq != Lk)
+        return fail(MHA_ERR_INVALID_ARG, "causal mask needs L_q == L_k (got %d, %d)", Lq, Lk);
+    if (mask->dense != nullptr && mask->dense_mq != 1 && mask->dense_mq != Lq)
+        return fail(MHA_ERR_INVALID_ARG, "dense_mq must be 1 or L_q (got %d)", mask->dense_mq);
+    return MHA_OK;
+}
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+// ==================================================================== C ABI
+extern "C" {
+
+const char* mha_version(void) { return "gb300-mha 0.1 (sm_103a)"; }
+
+const char* mha_last_error(void) { return g_last_error.c_str(); }
+
+size_t mha_workspace_size(mha_dtype_t dt, int B, int L_q, int L_k, int d_model, int h) {
+    Layout L;
+    if (!layout_of(dt, B, L_q, L_k, d_model, h, &L)) return 0;
+    return L.total;
+}
+
+mha_status_t mha_qkv_projection(mha_dtype_t dt, const void* query, const void* key, const void* value,
+                                const void* w_q, const void* b_q, const void* w_k, const void* b_k,
+                                const void* w_v, const void* b_v, int B, int L_q, int L_k, int d_model, int h,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+    mha_status_t st = check_sizes(dt, B, L_q, L_k, d_model, h);
+    if (st != MHA_OK) return st;
+    if (!query || !key || !value || !w_q || !w_k || !w_v)
+        return fail(MHA_ERR_INVALID_ARG, "query, key, value and W_q, W_k, W_v must not be NULL");
+    Layout L;
+    if ((st = check_workspace(dt, B, L_q, L_k, d_model, h, workspace, workspace_bytes, &L)) != MHA_OK) return st;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const int dk = d_model / h;
+    const cudaStream_t s = as_stream(stream);
+
+    if (dt == MHA_F32) {
+        mha::F32GemmParams p{};
+        const void* A[3] = {query, key, value};
+        const void* W[3] = {w_q, w_k, w_v};
+        const void* bias[3] = {b_q, b_k, b_v};
+        // Q -> Qh (its own [B, h, Lq, dk]); K, V -> KVh [B, 2h, Lk, dk] -- one launch, two layouts:
+        // the Q group writes with slabs = h, so it runs as a separate launch.
+        for (int g = 0; g < 3; ++g) {
+            p.g[g].A = static_cast<const float*>(A[g]);
+            p.g[g].W = static_cast<const float*>(W[g]);
+            p.g[g].bias = static_cast<const float*>(bias[g]);
+        }
+        p.B = B;
+        p.K = d_model;
+        p.N = d_model;
+        p.dk = dk;
+        p.out_plain = 0;
+        mha::F32GemmParams pq = p;
+        pq.ngroups = 1;
+        pq.slabs = h;
+        pq.g[0].out = reinterpret_cast<float*>(ws + L.q);
+        pq.g[0].L = L_q;
+        pq.g[0].out_j0 = 0;
+        cudaError_t e = mha::launch_gemm_f32(pq, s);
+        if (e != cudaSuccess) return cuda_fail(e, "Q projection launch");
+        mha::F32GemmParams pkv = p;
+        pkv.ngroups = 2;
+        pkv.slabs = 2 * h;
+        pkv.g[0] = p.g[1];
+        pkv.g[1] = p.g[2];
+        for (int g = 0; g < 2; ++g) {
+            pkv.g[g].out = reinterpret_cast<float*>(ws + L.kv);
+            pkv.g[g].L = L_k;
+            pkv.g[g].out_j0 = g * h;
+        }
+        e = mha::launch_gemm_f32(pkv, s);
+        if (e != cudaSuccess) return cuda_fail(e, "K/V projection launch");
+        return MHA_OK;
+    }
+
+    // ---- bf16: one tensor-core launch, three groups
+    const void* ptrs[9] = {query, key, value, w_q, w_k, w_v, b_q, b_k, b_v};
+    for (const void* ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return fail(MHA_ERR_INVALID_ARG, "bf16 tensors must be 16-byte aligned");
+    if ((st = get_encoder()) != MHA_OK) return st;
+    mha::GemmParams p;
+    memset(&p, 0, sizeof(p));
+    const void* A[3] = {query, key, value};
+    const void* W[3] = {w_q, w_k, w_v};
+    const void* bias[3] = {b_q, b_k, b_v};
+    const int Ls[3] = {L_q, L_k, L_k};
+    int max_m = 0;
+    for (int g = 0; g < 3; ++g) {
+        if ((st = map_rows(&p.a[g], A[g], B, Ls[g], d_model, "projection input")) != MHA_OK) return st;
+        if ((st = map_weight(&p.w[g], W[g], d_model, d_model)) != MHA_OK) return st;
+        if (g == 0) {
+            if ((st = map_heads4(&p.out[g], ws + L.q, B, h, L_q)) != MHA_OK) return st;
+        } else {
+            if ((st = map_heads4(&p.out[g], ws + L.kv, B, 2 * h, L_k)) != MHA_OK) return st;
+        }
+        p.g[g].L = Ls[g];
+        p.g[g].tiles_per_b = (Ls[g] + mha::kGemmBM - 1) / mha::kGemmBM;
+        p.g[g].m_tiles = B * p.g[g].tiles_per_b;
+        p.g[g].out_j0 = (g == 2) ? h : 0;
+        p.g[g].bias = static_cast<const __nv_bfloat16*>(bias[g]);
+        max_m = std::max(max_m, p.g[g].m_tiles);
+    }
+    p.ngroups = 3;
+    p.K = d_model;
+    p.N = d_model;
+    p.out_plain = 0;
+    p.status = device_status_ptr();
+    if (!p.status) return fail(MHA_ERR_CUDA, "device status word unavailable");
+    cudaError_t e = mha::launch_gemm_tc(p, max_m, s);
+    if (e != cudaSuccess) return cuda_fail(e, "QKV projection launch");
+    return MHA_OK;
+}
+
+mha_status_t mha_attention_core(mha_dtype_t dt, int B, int L_q, int L_k, int d_model, int h,
+                                const mha_mask_t* mask, float* p_attn, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+    mha_status_t st = check_sizes(dt, B, L_q, L_k, d_model, h);
+    if (st != MHA_OK) return st;
+    if ((st = check_mask(mask, L_q, L_k)) != MHA_OK) return st;
+    Layout L;
+    if ((st = check_workspace(dt, B, L_q, L_k, d_model, h, workspace, workspace_bytes, &L)) != MHA_OK) return st;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const int dk = d_model / h;
+    const cudaStream_t s = as_stream(stream);
+    const int causal = mask ? (mask->causal != 0) : 0;
+    const int32_t* vl = mask ? mask->key_valid_lens : nullptr;
+    const uint8_t* dense = mask ? mask->dense : nullptr;
+    const int dmq = (mask && mask->dense) ? mask->dense_mq : 0;
+
+    if (dt == MHA_F32) {
+        mha::F32AttnParams p{};
+        p.q = reinterpret_cast<const float*>(ws + L.q);
+        p.kv = reinterpret_cast<const float*>(ws + L.kv);
+        p.ctx = reinterpret_cast<float*>(ws + L.ctx);
+        p.p_attn = p_attn;
+        p.B = B; p.h = h; p.Lq = L_q; p.Lk = L_k; p.dk = dk;
+        p.causal = causal; p.valid_lens = vl; p.dense = dense; p.dense_mq = dmq;
+        cudaError_t e = mha::launch_attn_f32(p, s);
+        if (e != cudaSuccess) return cuda_fail(e, "fp32 attention launch");
+        return MHA_OK;
+    }
+
+    if ((st = get_encoder()) != MHA_OK) return st;
+    mha::AttnParams p;
+    memset(&p, 0, sizeof(p));
+    if ((st = map_heads3(&p.q_map, ws + L.q, B * h, L_q)) != MHA_OK) return st;
+    if ((st = map_heads3(&p.kv_map, ws + L.kv, B * 2 * h, L_k)) != MHA_OK) return st;
+    if ((st = map_rows(&p.ctx_map, ws + L.ctx, B, L_q, d_model, "context")) != MHA_OK) return st;
+    p.B = B; p.h = h; p.Lq = L_q; p.Lk = L_k;
+    p.causal = causal; p.valid_lens = vl; p.dense = dense; p.dense_mq = dmq;
+    p.stats = p_attn ? reinterpret_cast<float*>(ws + L.stat) : nullptr;
+    p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(dk)));
+    p.q_pairs = (L_q + 2 * mha::kAttnBM - 1) / (2 * mha::kAttnBM);
+    p.status = device_status_ptr();
+    if (!p.status) return fail(MHA_ERR_CUDA, "device status word unavailable");
+    cudaError_t e = mha::launch_attn_tc(p, s);
+    if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+    if (p_attn) {
+        mha::PattnParams pp{};
+        pp.q = reinterpret_cast<const __nv_bfloat16*>(ws + L.q);
+        pp.kv = reinterpret_cast<const __nv_bfloat16*>(ws + L.kv);
+        pp.stats = p.stats;
+        pp.p_attn = p_attn;
+        pp.B = B; pp.h = h; pp.Lq = L_q; pp.Lk = L_k;
+        pp.causal = causal; pp.valid_lens = vl; pp.dense = dense; pp.dense_mq = dmq;
+        pp.scale_log2 = p.scale_log2;
+        e = mha::launch_pattn_bf16(pp, s);
+        if (e != cudaSuccess) return cuda_fail(e, "p_attn launch");
+    }
+    return MHA_OK;
+}
+
+mha_status_t mha_output_projection(mha_dtype_t dt, const void* w_o, const void* b_o, int B, int L_q, int L_k,
+                                   int d_model, int h, void* out, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
+    mha_status_t st = check_sizes(dt, B, L_q, L_k, d_model, h);
+    if (st != MHA_OK) return st;
+    if (!w_o || !out) return fail(MHA_ERR_INVALID_ARG, "W_o and out must not be NULL");
+    Layout L;
+    if ((st = check_workspace(dt, B, L_q, L_k, d_model, h, workspace, workspace_bytes, &L)) != MHA_OK) return st;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const cudaStream_t s = as_stream(stream);
+
+    if (dt == MHA_F32) {
+        mha::F32GemmParams p{};
+        p.ngroups = 1;
+        p.B = B; p.K = d_model; p.N = d_model; p.dk = d_model / h; p.slabs = 1; p.out_plain = 1;
+        p.g[0].A = reinterpret_cast<const float*>(ws + L.ctx);
+        p.g[0].W = static_cast<const float*>(w_o);
+        p.g[0].bias = static_cast<const float*>(b_o);
+        p.g[0].out = static_cast<float*>(out);
+        p.g[0].L = L_q;
+        cudaError_t e = mha::launch_gemm_f32(p, s);
+        if (e != cudaSuccess) return cuda_fail(e, "fp32 output projection launch");
+        return MHA_OK;
+    }
+    if (!aligned16(w_o) || !aligned16(out) || (b_o && !aligned16(b_o)))
+        return fail(MHA_ERR_INVALID_ARG, "bf16 tensors must be 16-byte aligned");
+    if ((st = get_encoder()) != MHA_OK) return st;
+    mha::GemmParams p;
+    memset(&p, 0, sizeof(p));
+    if ((st = map_rows(&p.a[0], ws + L.ctx, B, L_q, d_model, "context")) != MHA_OK) return st;
+    if ((st = map_weight(&p.w[0], w_o, d_model, d_model)) != MHA_OK) return st;
+    if ((st = map_rows(&p.out[0], out, B, L_q, d_model, "output")) != MHA_OK) return st;
+    p.g[0].L = L_q;
+    p.g[0].tiles_per_b = (L_q + mha::kGemmBM - 1) / mha::kGemmBM;
+    p.g[0].m_tiles = B * p.g[0].tiles_per_b;
+    p.g[0].bias = static_cast<const __nv_bfloat16*>(b_o);
+    p.ngroups = 1;
+    p.K = d_model;
+    p.N = d_model;
+    p.out_plain = 1;
+    p.status = device_status_ptr();
+    if (!p.status) return fail(MHA_ERR_CUDA, "device status word unavailable");
+    cudaError_t e = mha::launch_gemm_tc(p, p.g[0].m_tiles, s);
+    if (e != cudaSuccess) return cuda_fail(e, "output projection launch");
+    return MHA_OK;
+}
+
+mha_status_t mha_forward(mha_dtype_t dt, const void* query, const void* key, const void* value, const void* w_q,
+                         const void* b_q, const void* w_k, const void* b_k, const void* w_v, const void* b_v,
+                         const void* w_o, const void* b_o, int B, int L_q, int L_k, int d_model, int h,
+                         const mha_mask_t* mask, void* out, float* p_attn, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+    // Validate everything before enqueueing anything.
+    mha_status_t st = check_sizes(dt, B, L_q, L_k, d_model, h);
+    if (st != MHA_OK) return st;
+    if ((st = check_mask(mask, L_q, L_k)) != MHA_OK) return st;
+    if (!query || !key || !value || !w_q || !w_k || !w_v || !w_o || !out)
+        return fail(MHA_ERR_INVALID_ARG, "query, key, value, W_q, W_k, W_v, W_o and out must not be NULL");
+    Layout L;
+    if ((st = check_workspace(dt, B, L_q, L_k, d_model, h, workspace, workspace_bytes, &L)) != MHA_OK) return st;
+    if (dt == MHA_BF16) {
+        const void* ptrs[13] = {query, key, value, w_q, w_k, w_v, w_o, b_q, b_k, b_v, b_o, out, p_attn};
+        for (const void* ptr : ptrs)
+            if (ptr && !aligned16(ptr)) return fail(MHA_ERR_INVALID_ARG, "bf16 tensors must be 16-byte aligned");
+    }
+    if ((st = mha_qkv_projection(dt, query, key, value, w_q, b_q, w_k, b_k, w_v, b_v, B, L_q, L_k, d_model, h,
+                                 workspace, workspace_bytes, stream)) != MHA_OK)
+        return st;
+    if ((st = mha_attention_core(dt, B, L_q, L_k, d_model, h, mask, p_attn, workspace, workspace_bytes, stream)) !=
+        MHA_OK)
+        return st;
+    return mha_output_projection(dt, w_o, b_o, B, L_q, L_k, d_model, h, out, workspace, workspace_bytes, stream);
+}
+
+size_t mha_host_staging_size(mha_dtype_t dt, int B, int L_q, int L_k, int d_model, int kv_distinct,
+                             int q_distinct) {
+    if (B <= 0 || L_q <= 0 || L_k <= 0 || d_model <= 0) return 0;
+    if (dt != MHA_F32 && dt != MHA_BF16) return 0;
+    const size_t es = dt == MHA_BF16 ? 2 : 4;
+    const size_t qb = align256(es * B * static_cast<size_t>(L_q) * d_model);
+    const size_t kb = align256(es * B * static_cast<size_t>(L_k) * d_model);
+    size_t total = qb /* query */ + qb /* out */;
+    if (q_distinct) total += kb;          // key not aliasing query
+    if (kv_distinct) total += kb;         // value not aliasing key
+    return total;
+}
+
+mha_status_t mha_forward_host(mha_dtype_t dt, const void* h_query, const void* h_key, const void* h_value,
+                              const void* w_q, const void* b_q, const void* w_k, const void* b_k, const void* w_v,
+                              const void* b_v, const void* w_o, const void* b_o, int B, int L_q, int L_k,
+                              int d_model, int h, const mha_mask_t* mask, void* h_out, void* staging,
+                              size_t staging_bytes, void* workspace, size_t workspace_bytes, void* stream) {
+    mha_status_t st = check_sizes(dt, B, L_q, L_k, d_model, h);
+    if (st != MHA_OK) return st;
+    if ((st = check_mask(mask, L_q, L_k)) != MHA_OK) return st;
+    if (!h_query || !h_key || !h_value || !h_out || !staging)
+        return fail(MHA_ERR_INVALID_ARG, "host query/key/value/out and staging must not be NULL");
+    const int q_distinct = h_key != h_query;
+    const int kv_distinct = h_value != h_key;
+    const size_t need = mha_host_staging_size(dt, B, L_q, L_k, d_model, kv_distinct, q_distinct);
+    if (staging_bytes < need) return fail(MHA_ERR_INVALID_ARG, "staging too small: %zu < %zu", staging_bytes, need);
+    if ((reinterpret_cast<uintptr_t>(staging) & 255u) != 0)
+        return fail(MHA_ERR_INVALID_ARG, "staging not 256-byte aligned");
+    const size_t es = dt == MHA_BF16 ? 2 : 4;
+    const size_t qbytes = es * B * static_cast<size_t>(L_q) * d_model;
+    const size_t kbytes = es * B * static_cast<size_t>(L_k) * d_model;
+    uint8_t* p = static_cast<uint8_t*>(staging);
+    uint8_t* d_q = p;
+    p += align256(qbytes);
+    uint8_t* d_out = p;
+    p += align256(qbytes);
+    uint8_t* d_k = d_q;
+    if (q_distinct) {
+        d_k = p;
+        p += align256(kbytes);
+    }
+    uint8_t* d_v = d_k;
+    if (kv_distinct) {
+        d_v = p;
+        p += align256(kbytes);
+    }
+    const cudaStream_t s = as_stream(stream);
+    cudaError_t e = cudaMemcpyAsync(d_q, h_query, qbytes, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess && q_distinct) e = cudaMemcpyAsync(d_k, h_key, kbytes, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess && kv_distinct) e = cudaMemcpyAsync(d_v, h_value, kbytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "host to device copy");
+    st = mha_forward(dt, d_q, d_k, d_v, w_q, b_q, w_k, b_k, w_v, b_v, w_o, b_o, B, L_q, L_k, d_model, h, mask, d_out,
+                     nullptr, workspace, workspace_bytes, stream);
+    if (st != MHA_OK) return st;
+    e = cudaMemcpyAsync(h_out, d_out, qbytes, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return cuda_fail(e, "device to host copy");
+    return MHA_OK;
+}
+
+mha_status_t mha_check_device_status(int* status, int reset) {
+    if (!status) return fail(MHA_ERR_INVALID_ARG, "status must not be NULL");
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "device synchronize");
+    int v = 0;
+    e = cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "status read");
+    *status = v;
+    if (reset) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int));
+        if (e != cudaSuccess) return cuda_fail(e, "status reset");
+    }
+    return MHA_OK;
+}
+
+}  // extern "C"

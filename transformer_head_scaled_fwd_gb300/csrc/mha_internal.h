@@ -1,0 +1,119 @@
+// mha_internal.h -- parameter blocks and launchers shared by the library's
+// translation units (not part of the public C ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace mha {
+
+// ------------------------------------------------------------ bf16 tensor-core GEMM
+// out[g] = A[g] . W[g]^T + bias[g] for up to three groups (the Q, K and V
+// projections share one launch). A[g] is [B, L_g, K]; tiles never straddle two
+// batch items, so rows past L_g inside a tile are zero-filled on load and
+// clipped on store.
+constexpr int kGemmBM = 128;
+constexpr int kGemmBN = 128;
+constexpr int kGemmBK = 64;
+constexpr int kGemmStages = 3;
+constexpr int kGemmThreads = 192;
+
+struct GemmGroup {
+    int L;             // rows per batch item
+    int tiles_per_b;   // ceil(L / 128)
+    int m_tiles;       // B * tiles_per_b
+    int out_j0;        // first 64-column slab of this group in a head-split output
+    const __nv_bfloat16* bias;   // [N] or nullptr
+};
+
+struct GemmParams {
+    CUtensorMap a[3];     // {K, L, B}, box {64, 128, 1}
+    CUtensorMap w[3];     // {K, N},    box {64, 128}
+    CUtensorMap out[3];   // head-split {64, L, slabs, B} box {64,128,1,1}, or plain {N, L, B} box {64,128,1}
+    GemmGroup g[3];
+    int ngroups;
+    int K;
+    int N;
+    int out_plain;        // 1: plain [B, L, N] output
+    int* status;
+};
+
+size_t gemm_tc_smem_bytes();
+cudaError_t launch_gemm_tc(const GemmParams& p, int max_m_tiles, cudaStream_t s);
+
+// ------------------------------------------------------------ bf16 tensor-core attention
+constexpr int kAttnBM = 128;       // queries per Q tile
+constexpr int kAttnBN = 128;       // keys per K/V tile
+constexpr int kAttnD = 64;         // head width d_k
+constexpr int kAttnStages = 3;     // K/V ring depth
+constexpr int kAttnThreads = 384;  // 2 softmax warpgroups (one per Q tile) + 1 warpgroup: TMA warp, MMA warp, 2 idle
+
+struct AttnParams {
+    CUtensorMap q_map;     // Qh as {64, L_q, B*h}
+    CUtensorMap kv_map;    // KVh as {64, L_k, B*2h}
+    CUtensorMap ctx_map;   // ctx as {d_model, L_q, B} (store)
+    int B, h, Lq, Lk;
+    int causal;
+    const int32_t* valid_lens;
+    const uint8_t* dense;
+    int dense_mq;
+    float* stats;          // [B, h, L_q, 2] (max in log2 units, sum) or nullptr
+    float scale_log2;      // log2(e) / sqrt(d_k)
+    int q_pairs;           // ceil(L_q / 256)
+    int* status;
+};
+
+size_t attn_tc_smem_bytes();
+cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t s);
+
+// p_attn for the bf16 path from Qh, KVh and the row statistics.
+struct PattnParams {
+    const __nv_bfloat16* q;     // Qh [B, h, Lq, 64]
+    const __nv_bfloat16* kv;    // KVh [B, 2, h, Lk, 64]
+    const float* stats;         // [B, h, Lq, 2]
+    float* p_attn;              // [B, h, Lq, Lk]
+    int B, h, Lq, Lk;
+    int causal;
+    const int32_t* valid_lens;
+    const uint8_t* dense;
+    int dense_mq;
+    float scale_log2;
+};
+cudaError_t launch_pattn_bf16(const PattnParams& p, cudaStream_t s);
+
+// ------------------------------------------------------------ fp32 SIMT path
+struct F32GemmGroup {
+    const float* A;      // [B, L, K]
+    const float* W;      // [N, K]
+    const float* bias;   // [N] or nullptr
+    float* out;          // head-split [B, slabs, L, dk] or plain [B, L, N]
+    int L;
+    int out_j0;
+};
+struct F32GemmParams {
+    F32GemmGroup g[3];
+    int ngroups;
+    int B, K, N;
+    int dk;
+    int slabs;           // slabs per batch item in a head-split output
+    int out_plain;
+};
+cudaError_t launch_gemm_f32(const F32GemmParams& p, cudaStream_t s);
+
+struct F32AttnParams {
+    const float* q;      // Qh [B, h, Lq, dk]
+    const float* kv;     // KVh [B, 2, h, Lk, dk]
+    float* ctx;          // [B, Lq, h*dk]
+    float* p_attn;       // [B, h, Lq, Lk] or nullptr
+    int B, h, Lq, Lk, dk;
+    int causal;
+    const int32_t* valid_lens;
+    const uint8_t* dense;
+    int dense_mq;
+};
+cudaError_t launch_attn_f32(const F32AttnParams& p, cudaStream_t s);
+
+}  // namespace mha
