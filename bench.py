@@ -1,0 +1,397 @@
+"""Benchmark of the multi-head attention forward pass on GB300.
+
+One step = the whole sublayer (Q/K/V projections + head split, fused attention
++ concat, output projection) over one batch of the long-sequence causal
+self-attention workload: B=4, L=8192, d_model=1024, h=16, d_k=64, causal mask,
+bf16 storage, fp32 accumulation, synthetic N(0,1) inputs and Xavier-uniform
+weights (seeded), inputs resident in HBM. The L2 cache (129 MB) is flushed
+before every timed step by writing a 256 MB buffer outside the timed events.
+
+Prints ONE JSON line (rank 0). ``value`` is algorithmic TFLOP/s (4 projection
+GEMMs + 4*d_k flops per allowed query/key pair per head) of the whole job.
+``--impl reference`` times the fp64 CPU oracle on a bounded causal-prefix
+sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MHA fwd TFLOP/s (bf16) and % of GB300 dense-BF16 peak; tokens/s"
+WORKLOAD = "long"
+DESCRIPTION = {
+    "enc": "encoder self-attention B32 L128 d_model512 h8 d_k64, key padding U{64..128}",
+    "dec": "decoder masked self-attention B32 L256 d_model512 h8 d_k64, causal AND key padding U{128..256}",
+    "xattn": "encoder-decoder attention B16 Lq256 Lk320 d_model1024 h16 d_k64, memory as key/value, padding U{160..320}",
+    "long": "long-sequence causal self-attention B4 L8192 d_model1024 h16 d_k64",
+}
+KERNEL_SOURCES = {"qkv_projection_gemm": "gemm_tc.cu", "attention_core": "attn_tc.cu",
+                  "output_projection_gemm": "gemm_tc.cu"}
+
+
+def source_digest(kernel: str) -> str:
+    import hashlib
+    csrc = os.path.join(ROOT, "transformer_head_scaled_fwd_gb300", "csrc")
+    h = hashlib.sha1()
+    for f in (KERNEL_SOURCES[kernel], "ptx.cuh", "mha_internal.h", "tmem_ldst.inc"):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum) recorded in a
+    profiles/*.md summary for this kernel and workload, if the kernel source is unchanged since."""
+    import glob
+    import re
+    pat = re.compile(r"<!-- bench-traffic kernel=(\S+) workload=(\S+) source_sha1=(\S+) bytes_per_launch=(\d+) -->")
+    for f in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        for m in pat.finditer(open(f).read()):
+            if m.group(1) == kernel and m.group(2) == workload and m.group(3) == source_digest(kernel):
+                return int(m.group(4))
+    return None
+
+
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+def algorithmic_flops(B, Lq, Lk, d, h, causal, valid_lens=None):
+    """4 projection GEMMs (2*M*N*K each) + 4*d_k flops per allowed (query, key) pair per head."""
+    dk = d // h
+    proj = 2.0 * d * d * (2 * B * Lq + 2 * B * Lk)
+    pairs = 0
+    for b in range(B):
+        vl = Lk if valid_lens is None else max(0, min(int(valid_lens[b]), Lk))
+        if causal:
+            # key j allowed iff j <= i and j < vl; with vl == 0 every key carries weight
+            if vl == 0:
+                pairs += Lq * Lk
+            else:
+                i = np.arange(Lq)
+                pairs += int(np.minimum(i + 1, vl).sum())
+        else:
+            pairs += Lq * (vl if vl > 0 else Lk)
+    attn = 4.0 * dk * pairs * h
+    return proj, attn
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms while the timed regions run."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu)], stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower() == "active"})
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(power) if power else None}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args):
+    """The fp64 oracle on the host cores, on a bounded causal-prefix sample of the workload."""
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    import oracle
+    from transformer_head_scaled_fwd_gb300 import workloads as W
+    oracle.build()
+    wl = W.WORKLOADS[WORKLOAD]
+    P = args.ref_prefix
+    inp = W.make_inputs(wl, B=1)
+    # A causal prefix of one sequence is a complete problem of its own: rows
+    # 0..P-1 of the full output depend only on tokens 0..P-1.
+    x = np.ascontiguousarray(inp.query[:, :P])
+    w = inp.weights
+    proj, attn = algorithmic_flops(1, P, P, wl.d_model, wl.h, True)
+    times = []
+    for s in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.mha_forward(x, x, x, w["w_q"], w["b_q"], w["w_k"], w["b_k"], w["w_v"], w["b_v"], w["w_o"],
+                           w["b_o"], wl.h, causal=True)
+        dt = time.perf_counter() - t0
+        if s >= args.warmup:
+            times.append(dt)
+    mean = sum(times) / len(times)
+    value = (proj + attn) / mean / 1e12
+    cores = oracle.num_threads()
+    sample = f"1 sequence, causal prefix of {P} tokens (d_model 1024, h 16), fp64, OpenMP"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "long-sequence causal self-attention B4 L8192 d_model1024 h16 d_k64 (oracle sample)",
+                   "B": 1, "seq_len": P, "d_model": wl.d_model, "h": wl.h, "causal": True},
+        "tokens_per_s": P / mean,
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(prefix: int):
+    import oracle
+    from transformer_head_scaled_fwd_gb300 import workloads as W
+    oracle.build()
+    wl = W.WORKLOADS[WORKLOAD]
+    inp = W.make_inputs(wl, B=1)
+    x = np.ascontiguousarray(inp.query[:, :prefix])
+    w = inp.weights
+    proj, attn = algorithmic_flops(1, prefix, prefix, wl.d_model, wl.h, True)
+    runs, t0 = 0, time.perf_counter()
+    while True:   # about 10 s of CPU work: repeat the sample
+        oracle.mha_forward(x, x, x, w["w_q"], w["b_q"], w["w_k"], w["b_k"], w["w_v"], w["b_v"], w["w_o"],
+                           w["b_o"], wl.h, causal=True)
+        runs += 1
+        dt = time.perf_counter() - t0
+        if dt >= 10.0 or runs >= 30:
+            break
+    return {"value": runs * (proj + attn) / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds": dt,
+            "sample": f"{runs} runs of 1 sequence, causal prefix of {prefix} tokens of the workload "
+                      f"(d_model 1024, h 16), fp64 C oracle, OpenMP"}
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    from transformer_head_scaled_fwd_gb300 import binding
+    from transformer_head_scaled_fwd_gb300 import build as B
+    from transformer_head_scaled_fwd_gb300 import workloads as W
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    B.build()
+    binding.load()
+    peaks, peak_src = load_peaks()
+
+    # CPU baseline first (rank 0, N=1 only), before any GPU work is timed.
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.ref_prefix)
+
+    wl = W.WORKLOADS[args.workload]
+    # weak scaling: every rank runs the full per-GPU batch with its own seed
+    inp = W.make_inputs(wl, seed_offset=rank)
+    dt = torch.bfloat16
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(f"cuda:{local}").to(dt)
+    q = dev(inp.query)
+    k = q if inp.key is inp.query else dev(inp.key)
+    v = k if inp.value is inp.key else dev(inp.value)
+    Wt = {n: dev(a) for n, a in inp.weights.items()}
+    Bn, Lq, d = inp.query.shape
+    Lk = inp.key.shape[1]
+    h = wl.h
+    vl = None if inp.valid_lens is None else torch.from_numpy(inp.valid_lens).cuda()
+    mask = binding.make_mask(wl.causal, vl, None)
+    ws = torch.empty(binding.workspace_size(binding.MHA_BF16, Bn, Lq, Lk, d, h), dtype=torch.uint8, device="cuda")
+    out = torch.empty(Bn, Lq, d, dtype=dt, device="cuda")
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    proj, attn = algorithmic_flops(Bn, Lq, Lk, d, h, wl.causal, inp.valid_lens)
+    flops = proj + attn
+
+    def step():
+        binding.mha_qkv_projection(q, k, v, Wt["w_q"], Wt["b_q"], Wt["w_k"], Wt["b_k"], Wt["w_v"], Wt["b_v"], h,
+                                   workspace=ws, stream=stream)
+        ev[1].record(stream)
+        binding.mha_attention_core(binding.MHA_BF16, Bn, Lq, Lk, d, h, workspace=ws, mask=mask, stream=stream)
+        ev[2].record(stream)
+        binding.mha_output_projection(Wt["w_o"], Wt["b_o"], Bn, Lq, Lk, h, out=out, workspace=ws, stream=stream)
+
+    K, Wm = args.steps, args.warmup
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K + Wm)]
+
+    # ---- end to end through the host-buffer entry point (pinned host in/out)
+    hq = torch.from_numpy(np.ascontiguousarray(inp.query)).to(dt).pin_memory()
+    hk = hq if inp.key is inp.query else torch.from_numpy(inp.key).to(dt).pin_memory()
+    hv = hk if inp.value is inp.key else torch.from_numpy(inp.value).to(dt).pin_memory()
+    hout = torch.empty(Bn, Lq, d, dtype=dt).pin_memory()
+    staging = torch.empty(binding.host_staging_size(binding.MHA_BF16, Bn, Lq, Lk, d, hv is not hk, hk is not hq),
+                          dtype=torch.uint8, device="cuda")
+    h2d = hq.numel() * 2 + (hk.numel() * 2 if hk is not hq else 0) + (hv.numel() * 2 if hv is not hk else 0)
+    d2h = hout.numel() * 2
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Wm + K)]
+
+    def e2e_step(s):
+        flush.zero_()
+        e2e_ev[s][0].record(stream)
+        binding.mha_forward_host(hq, hk, hv, Wt["w_q"], Wt["b_q"], Wt["w_k"], Wt["b_k"], Wt["w_v"], Wt["b_v"],
+                                 Wt["w_o"], Wt["b_o"], h, h_out=hout, staging=staging, workspace=ws, mask=mask,
+                                 stream=stream)
+        e2e_ev[s][1].record(stream)
+
+    # warm-up (untimed): device steps and host-buffer steps
+    for s in range(Wm):
+        ev = evs[s]
+        flush.zero_()
+        ev[0].record(stream)
+        step()
+        ev[3].record(stream)
+        e2e_step(s)
+    torch.cuda.synchronize()
+
+    launches = 0
+    with ClockSampler(local) as clk:
+        time.sleep(0.3)                        # let the sampler start
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for s in range(Wm, Wm + K):
+            ev = evs[s]
+            flush.zero_()                      # evict L2 between steps (outside the events)
+            ev[0].record(stream)
+            step()
+            ev[3].record(stream)
+            launches += 3
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        for s in range(Wm, Wm + K):
+            e2e_step(s)
+            launches += 3
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    status = binding.mha_check_device_status(reset=True)
+    if status != 0:
+        raise RuntimeError(f"a pipeline wait gave up inside a kernel (status 0x{status:x})")
+    timed = evs[Wm:]
+    step_ms = [e[0].elapsed_time(e[3]) for e in timed]
+    qkv_ms = [e[0].elapsed_time(e[1]) for e in timed]
+    att_ms = [e[1].elapsed_time(e[2]) for e in timed]
+    out_ms = [e[2].elapsed_time(e[3]) for e in timed]
+    total_ms = sum(step_ms)
+    e2e_total = sum(a.elapsed_time(b) for a, b in e2e_ev[Wm:])
+    if world > 1:
+        t = torch.tensor([total_ms, e2e_total], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, e2e_total = float(t[0].item()), float(t[1].item())
+    ms_per_step = total_ms / K
+    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    e2e_ms = e2e_total / K
+    e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
+
+    # ---- roofline of the dominant kernel (largest share of the step)
+    shares = {"qkv_projection_gemm": statistics.mean(qkv_ms), "attention_core": statistics.mean(att_ms),
+              "output_projection_gemm": statistics.mean(out_ms)}
+    dom = max(shares, key=shares.get)
+    dom_flops = {"qkv_projection_gemm": 0.75 * proj, "attention_core": attn, "output_projection_gemm": 0.25 * proj}
+    achieved = dom_flops[dom] / (shares[dom] * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    clocks = clk.summary()
+    traffic = committed_traffic(dom, args.workload)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": Wm,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1) activations, Xavier-uniform weights)",
+        "config": {"workload": DESCRIPTION[args.workload],
+                   "B_per_gpu": Bn, "global_batch": Bn * world, "seq_len": Lq, "d_model": d, "h": h,
+                   "mask": ("causal" if wl.causal else "") + (" key padding" if vl is not None else ""),
+                   "parallelism": f"dp{world} (batch sharded, no collective)",
+                   "l2": "flushed before every step (256 MB write outside the timed events)"},
+        "tokens_per_s": world * Bn * Lq / (ms_per_step * 1e-3),
+        "pct_of_bf16_peak": 100.0 * value / peak,
+        "stage_ms": {k2: round(v2, 4) for k2, v2 in shares.items()},
+        "roofline": {"kernel": dom, "source_sha1": source_digest(dom), "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} bf16_tflops (burst); sustained {peaks.get('bf16_tflops_sustained')}"},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "api": "mha_forward_host (pinned host query in, out back)"},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", default=WORKLOAD, choices=["enc", "dec", "xattn", "long"])
+    ap.add_argument("--ref-prefix", type=int, default=2048, help="causal prefix length of the oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl != "reference":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -126,8 +126,9 @@ def make_inputs(wl: Workload, *, bias_scale: float = 0.0, seed_offset: int = 0,
         v = k
         w = {n: round_bf16(t) for n, t in w.items()}
     to_np = lambda t: t.contiguous().numpy()
-    kn = to_np(k)
-    return Inputs(wl, to_np(q), kn, kn if v is k else to_np(v),
+    qn = to_np(q)
+    kn = qn if k is q else to_np(k)           # aliasing is kept: self-attention passes one tensor
+    return Inputs(wl, qn, kn, kn if v is k else to_np(v),
                   {n: to_np(t) for n, t in w.items()},
                   None if vl is None else vl.numpy())
 
@@ -155,9 +156,10 @@ def random_case(seed: int, B: int, Lq: int, Lk: int, d_model: int, h: int, *,
         v = k if (self_attn or kv_alias) else round_bf16(v)
         w = {n: round_bf16(t) for n, t in w.items()}
     vl = None if valid_lens is None else np.asarray(valid_lens, dtype=np.int32)
-    kn = k.contiguous().numpy()
+    qn = q.contiguous().numpy()
+    kn = qn if k is q else k.contiguous().numpy()
     vn = kn if v is k else v.contiguous().numpy()
-    return Inputs(wl, q.contiguous().numpy(), kn, vn,
+    return Inputs(wl, qn, kn, vn,
                   {n: t.contiguous().numpy() for n, t in w.items()}, vl)
 
 
