@@ -164,6 +164,40 @@ mha_status_t mha_forward_host(mha_dtype_t dt,
                               void* workspace, size_t workspace_bytes,
                               void* stream);
 
+/*
+ * mha_forward_noalloc -- mha_forward for callers that cannot allocate device
+ * memory. (The pages have no counterpart: this is an interface choice of this
+ * library.) Some callers are handed only their inputs and outputs: a plugin
+ * whose host application owns all device memory through its own pool, a
+ * serving path that must never hit cudaMalloc (which can synchronise the whole
+ * device), an interface with no workspace argument. This entry point takes the
+ * same arguments as mha_forward minus the workspace, allocates nothing, and
+ * uses a fixed scratch area built into the library instead:
+ *   - MHA_NOALLOC_SCRATCH_BYTES (48 MiB) of device memory, reserved on every
+ *     GPU that loads this part of the library and held until the process exits.
+ *   - Problems whose mha_workspace_size(...) exceeds it are rejected with
+ *     MHA_ERR_INVALID_ARG and a message naming both sizes (e.g. the encoder,
+ *     decoder and cross-attention workloads of this library fit; B=4, L=8192,
+ *     d_model=1024 does not).
+ *   - The first call on each device looks up the scratch address with that
+ *     device current; make that first call before any stream capture begins.
+ *   - All calls on a device share the one scratch area: calls whose work
+ *     overlaps on the GPU (other streams, other host threads) race and corrupt
+ *     each other. Serialise them, e.g. on one stream.
+ *   - Nothing in the scratch needs to start at zero; it is not cleared.
+ */
+#define MHA_NOALLOC_SCRATCH_BYTES ((size_t)48 << 20)
+mha_status_t mha_forward_noalloc(mha_dtype_t dt,
+                                 const void* query, const void* key, const void* value,
+                                 const void* w_q, const void* b_q,
+                                 const void* w_k, const void* b_k,
+                                 const void* w_v, const void* b_v,
+                                 const void* w_o, const void* b_o,
+                                 int B, int L_q, int L_k, int d_model, int h,
+                                 const mha_mask_t* mask,
+                                 void* out, float* p_attn,
+                                 void* stream);
+
 /* Message for the last non-OK status returned on this thread ("" if none). */
 const char* mha_last_error(void);
 

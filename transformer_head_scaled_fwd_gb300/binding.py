@@ -24,7 +24,7 @@ MHA_F32, MHA_BF16 = 0, 1
 # every symbol include/mha.h declares
 EXPORTS = ("mha_workspace_size", "mha_forward", "mha_qkv_projection", "mha_attention_core",
            "mha_output_projection", "mha_host_staging_size", "mha_forward_host", "mha_last_error",
-           "mha_check_device_status", "mha_version")
+           "mha_check_device_status", "mha_version", "mha_forward_noalloc")
 
 
 class MHAError(RuntimeError):
@@ -74,6 +74,8 @@ def load(path: str | None = None):
         lib.mha_check_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), i]
         lib.mha_version.restype = ctypes.c_char_p
         lib.mha_version.argtypes = []
+        lib.mha_forward_noalloc.restype = i
+        lib.mha_forward_noalloc.argtypes = [i] + [vp] * 11 + [i] * 5 + [ctypes.POINTER(MaskT), vp, vp, vp]
         _lib = lib
         return lib
 
@@ -172,6 +174,17 @@ def mha_forward_host(h_query, h_key, h_value, w_q, b_q, w_k, b_k, w_v, b_v, w_o,
         ctypes.byref(mask) if mask is not None else None, _ptr(h_out), _ptr(staging),
         staging.numel() * staging.element_size(), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def mha_forward_noalloc(query, key, value, w_q, b_q, w_k, b_k, w_v, b_v, w_o, b_o, h, *, out,
+                        mask=None, p_attn=None, stream=None):
+    """mha_forward without a workspace: uses the library's fixed scratch (see include/mha.h)."""
+    B, Lq, d = query.shape
+    Lk = key.shape[1]
+    _check(load().mha_forward_noalloc(
+        _dtype_code(query), _ptr(query), _ptr(key), _ptr(value), _ptr(w_q), _ptr(b_q), _ptr(w_k),
+        _ptr(b_k), _ptr(w_v), _ptr(b_v), _ptr(w_o), _ptr(b_o), B, Lq, Lk, d, h,
+        ctypes.byref(mask) if mask is not None else None, _ptr(out), _ptr(p_attn), _stream(stream)))
 
 
 def mha_check_device_status(reset: bool = True) -> int:

@@ -161,6 +161,8 @@ cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
 }  // namespace
 
+void mha::set_last_error(const char* msg) { g_last_error = msg; }
+
 // ==================================================================== C ABI
 extern "C" {
 

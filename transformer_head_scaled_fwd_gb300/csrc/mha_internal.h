@@ -10,6 +10,9 @@
 
 namespace mha {
 
+// Sets the message mha_last_error() returns on this thread.
+void set_last_error(const char* msg);
+
 // ------------------------------------------------------------ bf16 tensor-core GEMM
 // out[g] = A[g] . W[g]^T + bias[g] for up to three groups (the Q, K and V
 // projections share one launch). A[g] is [B, L_g, K]; tiles never straddle two
