@@ -14,24 +14,28 @@
 // softmax-then-matmul: the L_q x L_k score matrix never leaves the chip.
 //
 // CTA = two 128-row query tiles (t = 0, 1) of one (batch, head); key tiles of 128.
-// Tensor memory (512 columns): S_t at columns [128t, 128t+128) (fp32 scores),
-// P_t (bf16 weights, two per column) overwrites the first 64 columns of S_t,
-// O_t (fp32 output accumulator) at columns [256 + 64t, 256 + 64t + 64).
+// Tensor memory (512 columns, no aliasing):
+//   S_0 [0,128)  S_1 [128,256)   fp32 scores
+//   P_0 [256,320) P_1 [320,384)  bf16 weights, two per column (A operand of P.V)
+//   O_0 [384,448) O_1 [448,512)  fp32 output accumulators
+// Because P has its own columns, the next score tile S_t(j+1) is computed while
+// the softmax of tile j is still running: the softmax releases S_t as soon as
+// it has loaded it, and only waits for P.V(j-1) (to reuse P_t / rescale O_t).
 // Warp roles:
 //   warps 0-3 / 4-7   softmax for query tile 0 / 1: one thread per query row.
-//                     tcgen05.ld the score row, scale to log2 units, apply the
-//                     -1e9 fill, update (m, l), rescale O when m grows by more
-//                     than 2^8 (lazy: exact, the final O / l uses the same m),
-//                     write P into tensor memory with tcgen05.st.
-//   warp 8            TMA: Q tiles once, K and V tiles through a 3-deep ring.
-//   warp 9            allocates tensor memory; tcgen05.mma from one thread: S_t = Q_t K^T (SS, M=128,
-//                     N=128), O_t += P_t V (A from tensor memory, V MN-major,
-//                     M=128, N=64), interleaved so one tile's softmax overlaps
-//                     the other tile's MMAs.
-//   warps 10-11       idle (they complete the third warpgroup).
+//                     tcgen05.ld the score row, release S, scale to log2 units,
+//                     apply the -1e9 fill, update (m, l), rescale O when m grows
+//                     by more than 2^8 (lazy: exact, the final O / l uses the
+//                     same m), write P with tcgen05.st.
+//   warp 8            TMA: Q tiles once, K and V tiles through a 4-deep ring.
+//   warps 9 / 10      tcgen05.mma issuers for query tile 0 / 1 (one thread each):
+//                     S_t = Q_t K^T (SS, M=128, N=128), O_t += P_t V (A from
+//                     tensor memory, V MN-major, M=128, N=64). Warp 9 also
+//                     allocates the tensor memory.
+//   warp 11           idle (it completes the third warpgroup).
 // Registers: launched at 168 per thread (384 threads); the third warpgroup
-// drops to 56 and the two softmax warpgroups rise to 224
-// (128*56 + 256*224 = 64512 = 384*168, the launch total).
+// drops to 64 and the two softmax warpgroups rise to 216
+// (128*64 + 256*216 = 63488 <= 384*168 = 64512, the launch total).
 #include <math_constants.h>
 
 #include "mha_internal.h"
@@ -42,8 +46,12 @@ namespace {
 
 constexpr uint32_t kTileBytes = 128 * 128;          // 128 rows x 64 bf16 = 16 KB
 constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;      // + 128 t
+constexpr uint32_t kColP = 256;    // + 64 t
+constexpr uint32_t kColO = 384;    // + 64 t
 constexpr float kMaskedLog2 = -1.0e9f * 1.4426950408889634f;   // the -1e9 fill, in log2 units
 constexpr float kRescaleThreshold = 8.0f;           // lazy rescale: only when m grows by > 2^8
+constexpr int kHeadGroup = 8;                       // (batch, head) pairs scheduled together
 
 struct AttnSmem {
     uint64_t q_full;
@@ -51,9 +59,10 @@ struct AttnSmem {
     uint64_t v_full[kAttnStages];
     uint64_t k_empty[kAttnStages];
     uint64_t v_empty[kAttnStages];
-    uint64_t s_full[2];
-    uint64_t p_full[2];
-    uint64_t o_full[2];
+    uint64_t s_full[2];    // S_t(j) computed                      (tcgen05.commit)
+    uint64_t s_free[2];    // S_t(j) loaded by the softmax         (128 arrivals)
+    uint64_t p_full[2];    // P_t(j) written, O_t rescaled         (128 arrivals)
+    uint64_t pv_done[2];   // P_t(j).V done: P_t free, O_t stable  (tcgen05.commit)
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -75,11 +84,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     AttnSmem* sm = reinterpret_cast<AttnSmem*>(base + kOffBar);
 
-    // Longest-first order: blocks are dispatched in index order, and with the
-    // causal mask the last query tiles carry the most key tiles.
+    // Block order: (batch, head) pairs in groups of kHeadGroup, so the CTAs in
+    // flight share the K/V of a few heads in L2; inside a group, longest first
+    // (with the causal mask the last query tiles carry the most key tiles).
     const int BH = p.B * p.h;
-    const int qp = p.q_pairs - 1 - static_cast<int>(blockIdx.x) / BH;
-    const int bh = static_cast<int>(blockIdx.x) % BH;
+    const int QP = p.q_pairs;
+    const int idx = static_cast<int>(blockIdx.x);
+    const int grp = idx / (kHeadGroup * QP);
+    const int g_heads = min(kHeadGroup, BH - grp * kHeadGroup);
+    const int r = idx - grp * kHeadGroup * QP;
+    const int qp = QP - 1 - r / g_heads;
+    const int bh = grp * kHeadGroup + r % g_heads;
     const int b = bh / p.h;
     const int head = bh - b * p.h;
     const int q0 = qp * 2 * kAttnBM;
@@ -113,13 +128,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
         for (int s = 0; s < kAttnStages; ++s) {
             mbar_init(&sm->k_full[s], 1);
             mbar_init(&sm->v_full[s], 1);
-            mbar_init(&sm->k_empty[s], 1);
-            mbar_init(&sm->v_empty[s], 1);
+            mbar_init(&sm->k_empty[s], 2);   // both MMA issuers commit every stage
+            mbar_init(&sm->v_empty[s], 2);
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(&sm->s_full[t], 1);
+            mbar_init(&sm->s_free[t], kAttnBM);
             mbar_init(&sm->p_full[t], kAttnBM);
-            mbar_init(&sm->o_full[t], 1);
+            mbar_init(&sm->pv_done[t], 1);
         }
         sm->abort_flag = 0;
         fence_barrier_init();
@@ -140,7 +156,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
     // The two register-budget regions never rejoin: each ends with its own
     // copy of the teardown barrier (id 3, all 384 threads).
     if (warp >= 8) {
-      regs_dec<56>();
+      regs_dec<64>();
       if (warp == 8) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
@@ -159,60 +175,60 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
                 tma_load_3d(&p.kv_map, &sm->v_full[s], base + kOffV + s * kTileBytes, 0, j * kAttnBN, v_slab);
             }
         }
-    } else if (warp == 9) {
-        // ------------------------------------------------ MMA issuer
+    } else if (warp == 9 || warp == 10) {
+        // ------------------------------------------------ MMA issuers, one per query tile
+        // Issuer t runs S_t(j) and P_t(j-1).V_{j-1} software-pipelined; the two
+        // issuers' dependent MMA chains interleave in the tensor pipe and each
+        // one's barrier waits overlap the other's MMAs. Both commit every K/V
+        // stage (the *_empty barriers count 2), also for key tiles their own
+        // query tile does not use, after waiting for that stage to be filled.
+        const int t = warp - 9;
         if (lane == 0 && n_all > 0) {
             constexpr uint32_t idesc_s = idesc_bf16(kAttnBM, kAttnBN, false, false);
             constexpr uint32_t idesc_o = idesc_bf16(kAttnBM, kAttnD, false, true);
-            const uint32_t q_addr = smem_u32(base + kOffQ);
+            const uint32_t qa = smem_u32(base + kOffQ) + t * kTileBytes;
             const uint32_t k_addr = smem_u32(base + kOffK);
             const uint32_t v_addr = smem_u32(base + kOffV);
-            auto issue_s = [&](int t, int s) {
-                const uint32_t qa = q_addr + t * kTileBytes;
-                const uint32_t ka = k_addr + s * kTileBytes;
-#pragma unroll
-                for (int k = 0; k < kAttnD / 16; ++k)
-                    mma_ss(tmem + t * 128, sdesc_sw128(qa + k * 32, 16, 1024), sdesc_sw128(ka + k * 32, 16, 1024),
-                           idesc_s, k > 0);
-                tc_commit(&sm->s_full[t]);
-            };
-            auto issue_pv = [&](int t, int s, bool acc) {
-                const uint32_t va = v_addr + s * kTileBytes;
-#pragma unroll
-                for (int k = 0; k < kAttnBN / 16; ++k)
-                    mma_ts(tmem + 256 + t * 64, tmem + t * 128 + k * 8, sdesc_sw128(va + k * 2048, 8192, 1024),
-                           idesc_o, (acc || k > 0) ? 1u : 0u);
-            };
-            mbar_wait(&sm->q_full, 0, abort_flag, p.status, 0x203);
-            mbar_wait(&sm->k_full[0], 0, abort_flag, p.status, 0x204);
-            tc_fence_after();
-            if (tw[0].n > 0) issue_s(0, 0);
-            if (tw[1].n > 0) issue_s(1, 0);
-            tc_commit(&sm->k_empty[0]);
-            for (int j = 0; j < n_all; ++j) {
-                const int s = j % kAttnStages;
-                const uint32_t ph = (j / kAttnStages) & 1;
-                const bool has_next = j + 1 < n_all;
-                const int s1 = (j + 1) % kAttnStages;
-                const uint32_t ph1 = ((j + 1) / kAttnStages) & 1;
-                mbar_wait(&sm->v_full[s], ph, abort_flag, p.status, 0x205);
-                if (has_next) mbar_wait(&sm->k_full[s1], ph1, abort_flag, p.status, 0x206);
-                tc_fence_after();
-#pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    if (j < tw[t].n) {
-                        mbar_wait(&sm->p_full[t], j & 1, abort_flag, p.status, 0x207);
+            const uint32_t d_s = tmem + kColS + t * 128;
+            const uint32_t a_p = tmem + kColP + t * 64;
+            const uint32_t d_o = tmem + kColO + t * 64;
+            const int n_t = tw[t].n;
+            if (n_t > 0) mbar_wait(&sm->q_full, 0, abort_flag, p.status, 0x203);
+            for (int j = 0; j <= n_all; ++j) {
+                if (j < n_all) {
+                    const int s = j % kAttnStages;
+                    mbar_wait(&sm->k_full[s], (j / kAttnStages) & 1, abort_flag, p.status, 0x204);
+                    if (j < n_t) {
+                        if (j > 0) mbar_wait(&sm->s_free[t], (j - 1) & 1, abort_flag, p.status, 0x20a);
                         tc_fence_after();
-                        issue_pv(t, s, j > 0);
-                        if (j == tw[t].n - 1) tc_commit(&sm->o_full[t]);
+                        const uint32_t ka = k_addr + s * kTileBytes;
+#pragma unroll
+                        for (int k = 0; k < kAttnD / 16; ++k)
+                            mma_ss(d_s, sdesc_sw128(qa + k * 32, 16, 1024), sdesc_sw128(ka + k * 32, 16, 1024),
+                                   idesc_s, k > 0);
+                        tc_commit(&sm->s_full[t]);
                     }
-                    if (j + 1 < tw[t].n) issue_s(t, s1);
+                    tc_commit(&sm->k_empty[s]);
                 }
-                tc_commit(&sm->v_empty[s]);
-                if (has_next) tc_commit(&sm->k_empty[s1]);
+                if (j >= 1) {
+                    const int jj = j - 1;
+                    const int s = jj % kAttnStages;
+                    mbar_wait(&sm->v_full[s], (jj / kAttnStages) & 1, abort_flag, p.status, 0x205);
+                    if (jj < n_t) {
+                        mbar_wait(&sm->p_full[t], jj & 1, abort_flag, p.status, 0x207);
+                        tc_fence_after();
+                        const uint32_t va = v_addr + s * kTileBytes;
+#pragma unroll
+                        for (int k = 0; k < kAttnBN / 16; ++k)
+                            mma_ts(d_o, a_p + k * 8, sdesc_sw128(va + k * 2048, 8192, 1024), idesc_o,
+                                   (jj > 0 || k > 0) ? 1u : 0u);
+                        tc_commit(&sm->pv_done[t]);
+                    }
+                    tc_commit(&sm->v_empty[s]);
+                }
             }
         }
-    }
+      }
     tc_fence_before();
     named_bar_sync(3, kAttnThreads);
     if (warp == 9) {
@@ -221,7 +237,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
         tmem_dealloc(tmem, kTmemCols);
     }
     } else {
-        regs_inc<224>();
+        regs_inc<216>();
         // ------------------------------------------------ softmax, one thread per query row
         const int t = warp >> 2;
         const int quarter = warp & 3;
@@ -229,8 +245,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
         const int qt0 = q0 + t * kAttnBM;
         const int qi = qt0 + row;
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t s_tmem = tmem + lane_off + t * 128;
-        const uint32_t o_tmem = tmem + lane_off + 256 + t * 64;
+        const uint32_t s_tmem = tmem + lane_off + kColS + t * 128;
+        const uint32_t p_tmem = tmem + lane_off + kColP + t * 64;
+        const uint32_t o_tmem = tmem + lane_off + kColO + t * 64;
         const int n = tw[t].n;
         float m = -CUDART_INF_F;
         float l = 0.0f;
@@ -240,8 +257,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
             __syncwarp();
             tc_fence_after();
             uint32_t u[128];   // raw fp32 scores of this row
-            tmem_ld_x64(s_tmem, *reinterpret_cast<uint32_t(*)[64]>(&u[0]));
-            tmem_ld_x64(s_tmem + 64, *reinterpret_cast<uint32_t(*)[64]>(&u[64]));
+            tmem_ld_x128(s_tmem, u);
+            tc_fence_before();
+            mbar_arrive(&sm->s_free[t]);   // S_t may now be overwritten by S_t(j+1)
             const int k0 = j * kAttnBN;
             const bool edge = (p.dense != nullptr) || (k0 + kAttnBN > vl) ||
                               (p.causal && k0 + kAttnBN - 1 > qt0);
@@ -277,13 +295,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
                 }
                 sc = 1.0f;
             }
-            float mt = __uint_as_float(u[0]);
+            // row max: 8 independent 3-input max chains of depth 8, then a small tree
+            float a8[8];
 #pragma unroll
-            for (int c = 1; c < 128; ++c) mt = fmaxf(mt, __uint_as_float(u[c]));
+            for (int k = 0; k < 8; ++k) {
+                float a = fmax3(__uint_as_float(u[16 * k]), __uint_as_float(u[16 * k + 1]),
+                                __uint_as_float(u[16 * k + 2]));
+#pragma unroll
+                for (int e = 3; e < 15; e += 2)
+                    a = fmax3(a, __uint_as_float(u[16 * k + e]), __uint_as_float(u[16 * k + e + 1]));
+                a8[k] = fmaxf(a, __uint_as_float(u[16 * k + 15]));
+            }
+            const float mt = fmax3(fmax3(a8[0], a8[1], a8[2]), fmax3(a8[3], a8[4], a8[5]), fmaxf(a8[6], a8[7]));
             const float m_new = fmaxf(m, mt * sc);
             if (j == 0) {
                 m = m_new;
             } else {
+                // P_t and O_t are busy until P.V(j-1) has completed
+                mbar_wait(&sm->pv_done[t], (j - 1) & 1, abort_flag, p.status, 0x20b);
+                __syncwarp();
+                tc_fence_after();
                 const bool grow = (m_new - m) > kRescaleThreshold;
                 if (__any_sync(0xffffffffu, grow)) {
                     const float alpha = grow ? ex2_approx(m - m_new) : 1.0f;
@@ -301,34 +332,43 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
                     }
                 }
             }
-            const float neg_m = -m;
-            float lsum = 0.0f;
+            // p = exp2(u * sc - m): packed FMA for the argument, MUFU ex2, packed sums in
+            // four independent accumulators, bf16 pairs stored into P_t.
+            const float2 sc2 = make_float2(sc, sc);
+            const float2 nm2 = make_float2(-m, -m);
+            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(u[32 * q4 + 2 * c]), sc, neg_m));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(u[32 * q4 + 2 * c + 1]), sc, neg_m));
-                    lsum += p0 + p1;
-                    pk[c] = pack_bf16x2(p0, p1);
+                    const int e = 32 * q4 + 2 * c;
+                    float2 x = ffma2(make_float2(__uint_as_float(u[e]), __uint_as_float(u[e + 1])), sc2, nm2);
+                    x.x = ex2_approx(x.x);
+                    x.y = ex2_approx(x.y);
+                    acc[c & 3] = fadd2(acc[c & 3], x);
+                    pk[c] = pack_bf16x2(x.x, x.y);
                 }
-                tmem_st_x16(s_tmem + q4 * 16, pk);
+                tmem_st_x16(p_tmem + q4 * 16, pk);
             }
-            l += lsum;
+            const float2 s01 = fadd2(acc[0], acc[1]);
+            const float2 s23 = fadd2(acc[2], acc[3]);
+            const float2 s4 = fadd2(s01, s23);
+            l += s4.x + s4.y;
             tc_fence_before();
             mbar_arrive(&sm->p_full[t]);
         }
 
         // ---------------- epilogue: O / l -> bf16 -> the head's slab of ctx
         if (n > 0) {
-            mbar_wait(&sm->o_full[t], 0, abort_flag, p.status, 0x209);
+            mbar_wait(&sm->pv_done[t], (n - 1) & 1, abort_flag, p.status, 0x209);
             __syncwarp();
             tc_fence_after();
             uint32_t o[64];
             tmem_ld_x64(o_tmem, o);
             const float inv = 1.0f / l;
-            // Q_t's tile is free (its last MMA completed before o_full): stage there.
+            // Q_t's tile is free (its last S MMA completed before the last softmax): stage there.
             const uint32_t stage = smem_u32(base + kOffQ + t * kTileBytes) + row * 128;
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch) {
