@@ -308,20 +308,45 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
             }
             const float mt = fmax3(fmax3(a8[0], a8[1], a8[2]), fmax3(a8[3], a8[4], a8[5]), fmaxf(a8[6], a8[7]));
             const float m_new = fmaxf(m, mt * sc);
+            // Lazy rescale decision (registers only): the reference max m moves
+            // only when the row max grows by more than 2^8.
+            float alpha = 1.0f;
+            bool grow = false;
             if (j == 0) {
                 m = m_new;
             } else {
+                grow = (m_new - m) > kRescaleThreshold;
+                if (grow) {
+                    alpha = ex2_approx(m - m_new);
+                    l *= alpha;
+                    m = m_new;
+                }
+            }
+            // p = exp2(u * sc - m): packed FMA for the argument, MUFU ex2, packed sums in
+            // four independent accumulators, bf16 pairs kept in registers.
+            const float2 sc2 = make_float2(sc, sc);
+            const float2 nm2 = make_float2(-m, -m);
+            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};
+            uint32_t pk[64];
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                float2 x = ffma2(make_float2(__uint_as_float(u[2 * c]), __uint_as_float(u[2 * c + 1])), sc2, nm2);
+                x.x = ex2_approx(x.x);
+                x.y = ex2_approx(x.y);
+                acc[c & 3] = fadd2(acc[c & 3], x);
+                pk[c] = pack_bf16x2(x.x, x.y);
+            }
+            const float2 s01 = fadd2(acc[0], acc[1]);
+            const float2 s23 = fadd2(acc[2], acc[3]);
+            const float2 s4 = fadd2(s01, s23);
+            l += s4.x + s4.y;
+            if (j > 0) {
                 // P_t and O_t are busy until P.V(j-1) has completed
                 mbar_wait(&sm->pv_done[t], (j - 1) & 1, abort_flag, p.status, 0x20b);
                 __syncwarp();
                 tc_fence_after();
-                const bool grow = (m_new - m) > kRescaleThreshold;
                 if (__any_sync(0xffffffffu, grow)) {
-                    const float alpha = grow ? ex2_approx(m - m_new) : 1.0f;
-                    if (grow) {
-                        l *= alpha;
-                        m = m_new;
-                    }
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
                         uint32_t o[16];
@@ -332,30 +357,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
                     }
                 }
             }
-            // p = exp2(u * sc - m): packed FMA for the argument, MUFU ex2, packed sums in
-            // four independent accumulators, bf16 pairs stored into P_t.
-            const float2 sc2 = make_float2(sc, sc);
-            const float2 nm2 = make_float2(-m, -m);
-            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                             make_float2(0.f, 0.f)};
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const int e = 32 * q4 + 2 * c;
-                    float2 x = ffma2(make_float2(__uint_as_float(u[e]), __uint_as_float(u[e + 1])), sc2, nm2);
-                    x.x = ex2_approx(x.x);
-                    x.y = ex2_approx(x.y);
-                    acc[c & 3] = fadd2(acc[c & 3], x);
-                    pk[c] = pack_bf16x2(x.x, x.y);
-                }
-                tmem_st_x16(p_tmem + q4 * 16, pk);
-            }
-            const float2 s01 = fadd2(acc[0], acc[1]);
-            const float2 s23 = fadd2(acc[2], acc[3]);
-            const float2 s4 = fadd2(s01, s23);
-            l += s4.x + s4.y;
+            for (int q4 = 0; q4 < 4; ++q4)
+                tmem_st_x16_nowait(p_tmem + q4 * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16 * q4]));
+            tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&sm->p_full[t]);
         }
