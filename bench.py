@@ -152,6 +152,29 @@ def dist_setup():
     return world, rank, local
 
 
+def rank_inputs(wl, rank: int):
+    """Weak scaling: every rank processes a full per-GPU batch of the workload, drawn
+    with its own seed (independent sequences, no data-path exchange between ranks)."""
+    from transformer_head_scaled_fwd_gb300 import workloads as W
+    return W.make_inputs(wl, seed_offset=rank)
+
+
+def job_times(local_total_ms: float, local_e2e_ms: float, world: int, device=None):
+    """Whole-job timing: the slowest rank's totals (max over ranks)."""
+    if world == 1:
+        return local_total_ms, local_e2e_ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([local_total_ms, local_e2e_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t[0].item()), float(t[1].item())
+
+
+def job_throughput(world: int, flops_per_rank: float, ms_per_step: float) -> float:
+    """TFLOP/s of the whole job: units all ranks processed / the max-over-ranks time."""
+    return world * flops_per_rank / (ms_per_step * 1e-3) / 1e12
+
+
 def run_reference(args):
     """The fp64 oracle on the host cores, on a bounded causal-prefix sample of the workload."""
     world, rank, _ = dist_setup()
@@ -239,7 +262,7 @@ def run_gpu(args):
 
     wl = W.WORKLOADS[args.workload]
     # weak scaling: every rank runs the full per-GPU batch with its own seed
-    inp = W.make_inputs(wl, seed_offset=rank)
+    inp = rank_inputs(wl, rank)
     dt = torch.bfloat16
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(f"cuda:{local}").to(dt)
     q = dev(inp.query)
@@ -328,16 +351,12 @@ def run_gpu(args):
     qkv_ms = [e[0].elapsed_time(e[1]) for e in timed]
     att_ms = [e[1].elapsed_time(e[2]) for e in timed]
     out_ms = [e[2].elapsed_time(e[3]) for e in timed]
-    total_ms = sum(step_ms)
-    e2e_total = sum(a.elapsed_time(b) for a, b in e2e_ev[Wm:])
-    if world > 1:
-        t = torch.tensor([total_ms, e2e_total], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, e2e_total = float(t[0].item()), float(t[1].item())
+    total_ms, e2e_total = job_times(sum(step_ms), sum(a.elapsed_time(b) for a, b in e2e_ev[Wm:]), world,
+                                    device="cuda")
     ms_per_step = total_ms / K
-    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    value = job_throughput(world, flops, ms_per_step)
     e2e_ms = e2e_total / K
-    e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
+    e2e_value = job_throughput(world, flops, e2e_ms)
 
     # ---- roofline of the dominant kernel (largest share of the step)
     shares = {"qkv_projection_gemm": statistics.mean(qkv_ms), "attention_core": statistics.mean(att_ms),
