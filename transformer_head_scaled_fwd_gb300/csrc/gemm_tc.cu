@@ -5,76 +5,100 @@
 // y = x W^T + b with W stored [out, in], for up to three groups per launch
 // (the Q, K and V projections). The head split of the same section
 // (view(B, L, h, d_k).transpose(1, 2)) is folded into the epilogue: each 64-wide
-// column slab of the tile is written by one TMA store straight into its head's
+// column slab of a tile is written by one TMA store straight into its head's
 // [L, d_k] plane, so no transpose kernel runs.
 //
-// CTA = one 128 x 128 output tile of one batch item (tiles never straddle a
-// batch boundary). Warp roles:
-//   warp 0     TMA producer: A and W k-blocks (64 wide, 128-byte swizzle) into a
-//              3-stage shared-memory ring guarded by full/empty mbarriers.
-//   warp 1     allocates 128 tensor-memory columns and issues tcgen05.mma
-//              (M=128, N=128, K=16) from one thread; tcgen05.commit frees stages.
-//   warps 2-5  epilogue: tcgen05.ld the fp32 accumulator, add bias, round to
-//              bf16, stage in swizzled shared memory, TMA-store 64-column slabs.
+// Persistent kernel: one CTA per SM walks the output tiles (128 x 256, never
+// straddling a batch item) in a static round robin. Warp roles:
+//   warp 0     TMA producer: A (128 x 64) and W (256 x 64) k-blocks, 128-byte
+//              swizzle, into a 4-stage ring that runs ahead across tiles.
+//   warp 1     allocates 512 tensor-memory columns (two 128 x 256 fp32
+//              accumulators) and issues tcgen05.mma (M=128, N=256, K=16) from
+//              one thread; tcgen05.commit frees ring stages and hands a finished
+//              accumulator to the epilogue.
+//   warps 2-5  epilogue: tcgen05.ld 64 columns at a time, add the bias, round to
+//              bf16, stage in swizzled shared memory (two slab buffers) and
+//              TMA-store; the accumulator is released as soon as it is read, so
+//              the next tile's MMAs overlap this tile's stores.
 #include "mha_internal.h"
 #include "ptx.cuh"
 
 namespace mha {
 namespace {
 
-constexpr uint32_t kTileABytes = kGemmBM * kGemmBK * 2;   // 16 KB
-constexpr uint32_t kTileBBytes = kGemmBN * kGemmBK * 2;   // 16 KB
+constexpr int BN = kGemmBN;                              // 256
+constexpr uint32_t kTileABytes = kGemmBM * kGemmBK * 2;  // 16 KB
+constexpr uint32_t kTileBBytes = BN * kGemmBK * 2;       // 32 KB
 constexpr uint32_t kStageBytes = kTileABytes + kTileBBytes;
-constexpr uint32_t kTmemCols = 128;
+constexpr uint32_t kSlabBytes = kGemmBM * 128;           // 128 rows x 64 bf16
+constexpr uint32_t kTmemCols = 512;
 
 struct GemmSmem {
-    // layout after the 1024-aligned stage ring
     uint64_t full[kGemmStages];
     uint64_t empty[kGemmStages];
-    uint64_t acc_full;
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
     uint32_t tmem_base;
     int abort_flag;
-    float bias[kGemmBN];
 };
 
-constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kGemmStages * kStageBytes + sizeof(GemmSmem);
+// [ring: stages x (A | B)] [2 staging slabs] [GemmSmem]
+constexpr uint32_t kOffStage = kGemmStages * kStageBytes;
+constexpr uint32_t kOffBar = kOffStage + 2 * kSlabBytes;
+constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kOffBar + sizeof(GemmSmem);
 
-__global__ void __launch_bounds__(kGemmThreads, 2) gemm_bf16_tc_kernel(const __grid_constant__ GemmParams p) {
+struct TileCoord {
+    int grp, b, l0, n0;
+};
+
+__device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, int tile, int n_tiles) {
+    TileCoord c;
+    int g = 0;
+    while (g + 1 < p.ngroups && tile >= p.g[g].m_tiles * n_tiles) {
+        tile -= p.g[g].m_tiles * n_tiles;
+        ++g;
+    }
+    const int mt = tile / n_tiles;
+    const int nt = tile - mt * n_tiles;
+    c.grp = g;
+    c.b = mt / p.g[g].tiles_per_b;
+    c.l0 = (mt - c.b * p.g[g].tiles_per_b) * kGemmBM;
+    c.n0 = nt * BN;
+    return c;
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    GemmSmem* sm = reinterpret_cast<GemmSmem*>(ring + kGemmStages * kStageBytes);
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    GemmSmem* sm = reinterpret_cast<GemmSmem*>(base + kOffBar);
 
-    const int grp = blockIdx.z;
-    const GemmGroup& G = p.g[grp];
-    const int mt = blockIdx.y;
-    if (mt >= G.m_tiles) return;   // whole CTA, before any barrier
-    const int b = mt / G.tiles_per_b;
-    const int l0 = (mt - b * G.tiles_per_b) * kGemmBM;
-    const int n0 = blockIdx.x * kGemmBN;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int kblocks = p.K / kGemmBK;
+    const int n_tiles = (p.N + BN - 1) / BN;
+    int total = 0;
+    for (int g = 0; g < p.ngroups; ++g) total += p.g[g].m_tiles * n_tiles;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kGemmStages; ++s) {
             mbar_init(&sm->full[s], 1);
             mbar_init(&sm->empty[s], 1);
         }
-        mbar_init(&sm->acc_full, 1);
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&sm->acc_full[a], 1);
+            mbar_init(&sm->acc_empty[a], 128);
+        }
         sm->abort_flag = 0;
         fence_barrier_init();
-        tma_prefetch_desc(&p.a[grp]);
-        tma_prefetch_desc(&p.w[grp]);
-        tma_prefetch_desc(&p.out[grp]);
+        for (int g = 0; g < p.ngroups; ++g) {
+            tma_prefetch_desc(&p.a[g]);
+            tma_prefetch_desc(&p.w[g]);
+            tma_prefetch_desc(&p.out[g]);
+        }
     }
     if (warp == 1) {
         tmem_alloc(&sm->tmem_base, kTmemCols);
         tmem_relinquish();
-    }
-    if (threadIdx.x >= 64) {
-        const int c = threadIdx.x - 64;   // 128 epilogue threads load the bias slice
-        const int n = n0 + c;
-        sm->bias[c] = (G.bias != nullptr && n < p.N) ? __bfloat162float(G.bias[n]) : 0.0f;
     }
     tc_fence_before();
     __syncthreads();
@@ -83,85 +107,104 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_bf16_tc_kernel(const __g
     volatile int* abort_flag = &sm->abort_flag;
 
     if (warp == 0) {
+        // ---------------- TMA producer
         if (lane == 0) {
-            for (int kb = 0; kb < kblocks; ++kb) {
-                const int s = kb % kGemmStages;
-                const uint32_t ph = (kb / kGemmStages) & 1;
-                mbar_wait(&sm->empty[s], ph ^ 1, abort_flag, p.status, 0x101);
-                uint8_t* a_dst = ring + s * kStageBytes;
-                uint8_t* b_dst = a_dst + kTileABytes;
-                mbar_arrive_expect_tx(&sm->full[s], kStageBytes);
-                tma_load_3d(&p.a[grp], &sm->full[s], a_dst, kb * kGemmBK, l0, b);
-                tma_load_2d(&p.w[grp], &sm->full[s], b_dst, kb * kGemmBK, n0);
+            int it = 0;   // ring position across tiles
+            for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+                const TileCoord c = tile_coord(p, tile, n_tiles);
+                for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                    const int s = it % kGemmStages;
+                    const uint32_t ph = (it / kGemmStages) & 1;
+                    mbar_wait(&sm->empty[s], ph ^ 1, abort_flag, p.status, 0x101);
+                    uint8_t* a_dst = base + s * kStageBytes;
+                    mbar_arrive_expect_tx(&sm->full[s], kStageBytes);
+                    tma_load_3d(&p.a[c.grp], &sm->full[s], a_dst, kb * kGemmBK, c.l0, c.b);
+                    tma_load_2d(&p.w[c.grp], &sm->full[s], a_dst + kTileABytes, kb * kGemmBK, c.n0);
+                }
             }
         }
     } else if (warp == 1) {
+        // ---------------- MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16(kGemmBM, kGemmBN, false, false);
-            for (int kb = 0; kb < kblocks; ++kb) {
-                const int s = kb % kGemmStages;
-                const uint32_t ph = (kb / kGemmStages) & 1;
-                mbar_wait(&sm->full[s], ph, abort_flag, p.status, 0x102);
+            constexpr uint32_t idesc = idesc_bf16(kGemmBM, BN, false, false);
+            int it = 0, use = 0;
+            for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++use) {
+                const int acc = use & 1;
+                const uint32_t d = tmem + acc * BN;
+                mbar_wait(&sm->acc_empty[acc], ((use >> 1) & 1) ^ 1, abort_flag, p.status, 0x104);
                 tc_fence_after();
-                const uint32_t a_addr = smem_u32(ring + s * kStageBytes);
-                const uint32_t b_addr = a_addr + kTileABytes;
+                for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                    const int s = it % kGemmStages;
+                    const uint32_t ph = (it / kGemmStages) & 1;
+                    mbar_wait(&sm->full[s], ph, abort_flag, p.status, 0x102);
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(base + s * kStageBytes);
+                    const uint32_t b_addr = a_addr + kTileABytes;
 #pragma unroll
-                for (int k = 0; k < kGemmBK / 16; ++k) {
-                    const uint64_t ad = sdesc_sw128(a_addr + k * 32, 16, 1024);
-                    const uint64_t bd = sdesc_sw128(b_addr + k * 32, 16, 1024);
-                    mma_ss(tmem, ad, bd, idesc, (kb | k) != 0);
+                    for (int k = 0; k < kGemmBK / 16; ++k)
+                        mma_ss(d, sdesc_sw128(a_addr + k * 32, 16, 1024), sdesc_sw128(b_addr + k * 32, 16, 1024),
+                               idesc, (kb | k) != 0);
+                    tc_commit(&sm->empty[s]);
                 }
-                tc_commit(&sm->empty[s]);
+                tc_commit(&sm->acc_full[acc]);
             }
-            tc_commit(&sm->acc_full);
         }
     } else {
         // ---------------- epilogue: warps 2..5, lane quarter = warp % 4
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
-        mbar_wait(&sm->acc_full, 0, abort_flag, p.status, 0x103);
-        __syncwarp();
-        tc_fence_after();
-        // The ring is idle now (all loads consumed, all MMAs complete): reuse it
-        // as the bf16 staging tile, two 64-column slabs of 128 rows x 128 bytes.
-        const uint32_t stage_addr = smem_u32(ring);
-#pragma unroll
-        for (int cb = 0; cb < kGemmBN / 32; ++cb) {
-            uint32_t v[32];
-            tmem_ld_x32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + cb * 32, v);
-            const int slab = cb >> 1;
-            const uint32_t slab_addr = stage_addr + slab * (kGemmBM * 128) + row * 128;
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int c = cb * 32 + u * 8 + e * 2;
-                    const float x0 = __uint_as_float(v[u * 8 + e * 2]) + sm->bias[c];
-                    const float x1 = __uint_as_float(v[u * 8 + e * 2 + 1]) + sm->bias[c + 1];
-                    w[e] = pack_bf16x2(x0, x1);
+        const bool issuer = (warp == 2 && lane == 0);
+        int use = 0, slabs_issued = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++use) {
+            const TileCoord c = tile_coord(p, tile, n_tiles);
+            const GemmGroup& G = p.g[c.grp];
+            const int acc = use & 1;
+            mbar_wait(&sm->acc_full[acc], (use >> 1) & 1, abort_flag, p.status, 0x103);
+            __syncwarp();
+            tc_fence_after();
+            const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+#pragma unroll 1
+            for (int slab = 0; slab < BN / 64; ++slab) {
+                const int n = c.n0 + slab * 64;
+                uint32_t v[64];
+                tmem_ld_x64(t_row + slab * 64, v);
+                if (slab == BN / 64 - 1) {
+                    // accumulator fully read: the next tile's MMAs may overwrite it
+                    tc_fence_before();
+                    mbar_arrive(&sm->acc_empty[acc]);
                 }
-                const int chunk = (cb & 1) * 4 + u;            // 16-byte chunk within the 128-byte row
-                const uint32_t addr = slab_addr + ((chunk ^ (row & 7)) << 4);
-                st_shared_v4(addr, w[0], w[1], w[2], w[3]);
-            }
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(1, 128);
-        if (warp == 2 && lane == 0 && !*abort_flag) {
+                if (n >= p.N) continue;   // uniform across the CTA
+                const int sb = slabs_issued & 1;
+                // the TMA store that last used this staging buffer must have read it
+                if (issuer && slabs_issued >= 2) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+                named_bar_sync(1, 128);
+                const uint32_t stage = smem_u32(base + kOffStage + sb * kSlabBytes) + row * 128;
 #pragma unroll
-            for (int slab = 0; slab < kGemmBN / 64; ++slab) {
-                const int n = n0 + slab * 64;
-                if (n >= p.N) break;
-                const uint8_t* src = ring + slab * (kGemmBM * 128);
-                if (p.out_plain)
-                    tma_store_3d(&p.out[grp], src, n, l0, b);
-                else
-                    tma_store_4d(&p.out[grp], src, 0, l0, G.out_j0 + n / 64, b);
+                for (int ch = 0; ch < 8; ++ch) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int cc = ch * 8 + 2 * e;
+                        const float b0 = G.bias ? __bfloat162float(G.bias[n + cc]) : 0.0f;
+                        const float b1 = G.bias ? __bfloat162float(G.bias[n + cc + 1]) : 0.0f;
+                        w[e] = pack_bf16x2(__uint_as_float(v[cc]) + b0, __uint_as_float(v[cc + 1]) + b1);
+                    }
+                    st_shared_v4(stage + ((ch ^ (row & 7)) << 4), w[0], w[1], w[2], w[3]);
+                }
+                fence_proxy_async_smem();
+                named_bar_sync(1, 128);
+                if (issuer && !*abort_flag) {
+                    const uint8_t* src = base + kOffStage + sb * kSlabBytes;
+                    if (p.out_plain)
+                        tma_store_3d(&p.out[c.grp], src, n, c.l0, c.b);
+                    else
+                        tma_store_4d(&p.out[c.grp], src, 0, c.l0, G.out_j0 + n / 64, c.b);
+                    tma_store_commit();
+                }
+                ++slabs_issued;
             }
-            tma_store_commit();
-            tma_store_wait_all();
         }
+        if (issuer) tma_store_wait_all();
     }
 
     tc_fence_before();
@@ -177,12 +220,19 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_bf16_tc_kernel(const __g
 
 size_t gemm_tc_smem_bytes() { return kSmemBytes; }
 
-cudaError_t launch_gemm_tc(const GemmParams& p, int max_m_tiles, cudaStream_t s) {
-    static_assert(kGemmBN == 128 && kGemmBM == 128, "epilogue assumes 128 x 128 tiles");
+cudaError_t launch_gemm_tc(const GemmParams& p, int /*max_m_tiles*/, cudaStream_t s) {
+    static_assert(kGemmBM == 128 && BN == 256, "epilogue assumes 128 x 256 tiles");
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
     cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
-    dim3 grid((p.N + kGemmBN - 1) / kGemmBN, max_m_tiles, p.ngroups);
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const int n_tiles = (p.N + BN - 1) / BN;
+    long total = 0;
+    for (int g = 0; g < p.ngroups; ++g) total += static_cast<long>(p.g[g].m_tiles) * n_tiles;
+    const int grid = static_cast<int>(total < sms ? total : sms);
     gemm_bf16_tc_kernel<<<grid, kGemmThreads, kSmemBytes, s>>>(p);
     return cudaGetLastError();
 }

@@ -91,11 +91,11 @@ mha_status_t map_rows(CUtensorMap* m, const void* base, int B, int L, int N, con
     const uint32_t box[3] = {64, 128, 1};
     return encode_bf16(m, base, 3, dims, str, box, what);
 }
-// weight [N, K] as {K, N}, box {64, 128}
+// weight [N, K] as {K, N}, box {64, kGemmBN}
 mha_status_t map_weight(CUtensorMap* m, const void* base, int N, int K) {
     const uint64_t dims[2] = {(uint64_t)K, (uint64_t)N};
     const uint64_t str[1] = {(uint64_t)K * 2};
-    const uint32_t box[2] = {64, 128};
+    const uint32_t box[2] = {64, (uint32_t)mha::kGemmBN};
     return encode_bf16(m, base, 2, dims, str, box, "weight");
 }
 // head-split [B, slabs, L, 64] as {64, L, slabs, B}, box {64, 128, 1, 1}

@@ -17,11 +17,11 @@ void set_last_error(const char* msg);
 // out[g] = A[g] . W[g]^T + bias[g] for up to three groups (the Q, K and V
 // projections share one launch). A[g] is [B, L_g, K]; tiles never straddle two
 // batch items, so rows past L_g inside a tile are zero-filled on load and
-// clipped on store.
+// clipped on store. Persistent: one CTA per SM walks the tiles.
 constexpr int kGemmBM = 128;
-constexpr int kGemmBN = 128;
+constexpr int kGemmBN = 256;
 constexpr int kGemmBK = 64;
-constexpr int kGemmStages = 3;
+constexpr int kGemmStages = 4;
 constexpr int kGemmThreads = 192;
 
 struct GemmGroup {
@@ -34,7 +34,7 @@ struct GemmGroup {
 
 struct GemmParams {
     CUtensorMap a[3];     // {K, L, B}, box {64, 128, 1}
-    CUtensorMap w[3];     // {K, N},    box {64, 128}
+    CUtensorMap w[3];     // {K, N},    box {64, 256}
     CUtensorMap out[3];   // head-split {64, L, slabs, B} box {64,128,1,1}, or plain {N, L, B} box {64,128,1}
     GemmGroup g[3];
     int ngroups;
