@@ -64,6 +64,8 @@ def _load():
             lib.oracle_linear.restype = None
             lib.oracle_linear.argtypes = [dp, dp, dp, ctypes.c_long, ctypes.c_int,
                                           ctypes.c_int, dp]
+            lib.oracle_ffn_forward.restype = ctypes.c_int
+            lib.oracle_ffn_forward.argtypes = [dp] * 5 + [ctypes.c_long, ctypes.c_int, ctypes.c_int, dp]
             lib.oracle_num_threads.restype = ctypes.c_int
             lib.oracle_num_threads.argtypes = []
             _lib = lib
@@ -138,3 +140,20 @@ def mha_forward(query, key, value, w_q, b_q, w_k, b_k, w_v, b_v, w_o, b_o, h,
     if rc != 0:
         raise ValueError(f"oracle_mha_forward rejected its arguments (code {rc})")
     return (out, p) if want_p_attn else out
+
+
+def ffn_forward(x, w_1, b_1, w_2, b_2):
+    """Position-wise FFN in fp64: max(0, x W_1^T + b_1) W_2^T + b_2 (nn.Linear layouts).
+    x [..., d_model]; w_1 [d_ff, d_model]; w_2 [d_model, d_ff]; b_* or None."""
+    lib = _load()
+    x = _f64(x)
+    w_1, b_1, w_2, b_2 = _f64(w_1), _f64(b_1), _f64(w_2), _f64(b_2)
+    d_ff, d_model = w_1.shape
+    rows = int(np.prod(x.shape[:-1]))
+    out = np.empty(x.shape[:-1] + (d_model,), dtype=np.float64)
+    rc = lib.oracle_ffn_forward(_ptr(x, ctypes.c_double), _ptr(w_1, ctypes.c_double), _ptr(b_1, ctypes.c_double),
+                                _ptr(w_2, ctypes.c_double), _ptr(b_2, ctypes.c_double), rows, d_model, d_ff,
+                                _ptr(out, ctypes.c_double))
+    if rc != 0:
+        raise ValueError(f"oracle_ffn_forward rejected its arguments (code {rc})")
+    return out

@@ -84,3 +84,11 @@ def mha_forward(query, key, value, w_q, b_q, w_k, b_k, w_v, b_v, w_o, b_o, h,
         out_all.append(linear(ctx, w_o, b_o))
         p_all.append(p_b)
     return out_all, p_all
+
+
+def ffn_forward(x, w_1, b_1, w_2, b_2):
+    """Position-wise FFN, nested lists: max(0, x W_1^T + b_1) W_2^T + b_2 per row
+    ("003-Transformer" tutorial, feed-forward layer)."""
+    hid = linear(x, w_1, b_1)
+    hid = [[v if v > 0.0 else 0.0 for v in row] for row in hid]
+    return linear(hid, w_2, b_2)

@@ -182,3 +182,26 @@ int oracle_num_threads(void)
     return 1;
 #endif
 }
+
+/*
+ * oracle_ffn_forward -- position-wise feed-forward network in fp64
+ * ("003-Transformer" tutorial, section on the feed-forward layer, and "From RNN
+ * to Attention", part 3, FFN: FFN(x) = max(0, x W_1 + b_1) W_2 + b_2, as
+ * PositionwiseFeedForward: w_1 = nn.Linear(d_model, d_ff), w_2 = nn.Linear(d_ff,
+ * d_model), relu between them; dropout is the identity).
+ * x [rows, d_model]; w_1 [d_ff, d_model]; w_2 [d_model, d_ff]; b_* or NULL.
+ * Returns 0, or 1 on non-positive sizes, 2 on allocation failure.
+ */
+int oracle_ffn_forward(const double* x, const double* w_1, const double* b_1,
+                       const double* w_2, const double* b_2,
+                       long rows, int d_model, int d_ff, double* out)
+{
+    if (rows <= 0 || d_model <= 0 || d_ff <= 0) return 1;
+    double* hid = (double*)malloc(sizeof(double) * (size_t)rows * d_ff);
+    if (!hid) return 2;
+    oracle_linear(x, w_1, b_1, rows, d_model, d_ff, hid);
+    for (long i = 0; i < rows * (long)d_ff; ++i) if (hid[i] < 0.0) hid[i] = 0.0;   /* relu */
+    oracle_linear(hid, w_2, b_2, rows, d_ff, d_model, out);
+    free(hid);
+    return 0;
+}
