@@ -394,6 +394,61 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+def run_gpu_ffn(args):
+    """Position-wise FFN (max(0, x W_1 + b_1) W_2 + b_2) on one GPU: TFLOP/s of the two GEMMs."""
+    import torch
+
+    from transformer_head_scaled_fwd_gb300 import binding
+    from transformer_head_scaled_fwd_gb300 import build as B
+    from transformer_head_scaled_fwd_gb300 import workloads as W
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    B.build()
+    binding.load()
+    peaks, peak_src = load_peaks()
+    cfg = W.FFN_WORKLOADS[args.ffn_workload]
+    inp = W.make_ffn_inputs(cfg["B"], cfg["L"], cfg["d_model"], cfg["d_ff"], seed=rank)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda().to(torch.bfloat16)
+    x, w1, b1, w2, b2 = dev(inp.x), dev(inp.w_1), dev(inp.b_1), dev(inp.w_2), dev(inp.b_2)
+    Bn, L, d = x.shape
+    d_ff = w1.shape[0]
+    ws = torch.empty(binding.ffn_workspace_size(binding.MHA_BF16, Bn, L, d, d_ff), dtype=torch.uint8,
+                     device="cuda")
+    out = torch.empty_like(x)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    flops = 4.0 * Bn * L * d * d_ff
+    K, Wm = args.steps, args.warmup
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K + Wm)]
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        for s_ in range(Wm + K):
+            flush.zero_()
+            evs[s_][0].record(stream)
+            binding.mha_ffn_forward(x, w1, b1, w2, b2, out=out, workspace=ws, stream=stream)
+            evs[s_][1].record(stream)
+        torch.cuda.synchronize()
+    if binding.mha_check_device_status(reset=True) != 0:
+        raise RuntimeError("a pipeline wait gave up inside a kernel")
+    ms = sum(a.elapsed_time(b) for a, b in evs[Wm:]) / K
+    value = flops / (ms * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    line = {
+        "metric": "FFN fwd TFLOP/s (bf16)", "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": K,
+        "warmup": Wm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1) activations, Xavier-uniform weights)",
+        "config": {"workload": f"position-wise FFN B{Bn} L{L} d_model{d} d_ff{d_ff}", "tokens": Bn * L,
+                   "l2": "flushed before every step"},
+        "tokens_per_s": Bn * L / (ms * 1e-3),
+        "roofline": {"kernel": "gemm_bf16_tc (2 launches)", "bound": "tensor", "achieved": value, "peak": peak,
+                     "unit": "TFLOP/s", "frac": value / peak, "traffic": None,
+                     "peak_source": f"{peak_src} bf16_tflops (burst)"},
+        "gpu_launches": 2 * K, "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -403,11 +458,16 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD, choices=["enc", "dec", "xattn", "long"])
     ap.add_argument("--ref-prefix", type=int, default=2048, help="causal prefix length of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", choices=["mha", "ffn"], default="mha",
+                    help="mha: the attention sublayer (default); ffn: the position-wise FFN")
+    ap.add_argument("--ffn-workload", default="ffn_long", choices=["ffn_base", "ffn_long"])
     args = ap.parse_args()
     if args.warmup < 3 and args.impl != "reference":
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.path == "ffn":
+        run_gpu_ffn(args)
     else:
         run_gpu(args)
 

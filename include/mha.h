@@ -198,6 +198,25 @@ mha_status_t mha_forward_noalloc(mha_dtype_t dt,
                                  void* out, float* p_attn,
                                  void* stream);
 
+/*
+ * Position-wise feed-forward network ("003-Transformer" tutorial, feed-forward
+ * layer; "From RNN to Attention", part 3, FFN):
+ *   out = max(0, x W_1^T + b_1) W_2^T + b_2        (dropout = identity)
+ *   x [B, L, d_model]; w_1 [d_ff, d_model], b_1 [d_ff] or NULL;
+ *   w_2 [d_model, d_ff], b_2 [d_model] or NULL; out [B, L, d_model], type dt.
+ *   MHA_BF16: d_model and d_ff multiples of 64, 16-byte aligned pointers; the
+ *   two layers run on the tensor-core GEMM (ReLU fused into the first epilogue).
+ *   The hidden activations [B, L, d_ff] live in the caller's workspace of at
+ *   least mha_ffn_workspace_size(...) bytes (256-byte aligned).
+ */
+size_t mha_ffn_workspace_size(mha_dtype_t dt, int B, int L, int d_model, int d_ff);
+mha_status_t mha_ffn_forward(mha_dtype_t dt, const void* x,
+                             const void* w_1, const void* b_1,
+                             const void* w_2, const void* b_2,
+                             int B, int L, int d_model, int d_ff,
+                             void* out, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
 /* Message for the last non-OK status returned on this thread ("" if none). */
 const char* mha_last_error(void);
 

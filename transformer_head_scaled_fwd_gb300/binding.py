@@ -24,7 +24,8 @@ MHA_F32, MHA_BF16 = 0, 1
 # every symbol include/mha.h declares
 EXPORTS = ("mha_workspace_size", "mha_forward", "mha_qkv_projection", "mha_attention_core",
            "mha_output_projection", "mha_host_staging_size", "mha_forward_host", "mha_last_error",
-           "mha_check_device_status", "mha_version", "mha_forward_noalloc")
+           "mha_check_device_status", "mha_version", "mha_forward_noalloc", "mha_ffn_workspace_size",
+           "mha_ffn_forward")
 
 
 class MHAError(RuntimeError):
@@ -74,6 +75,10 @@ def load(path: str | None = None):
         lib.mha_check_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), i]
         lib.mha_version.restype = ctypes.c_char_p
         lib.mha_version.argtypes = []
+        lib.mha_ffn_workspace_size.restype = sz
+        lib.mha_ffn_workspace_size.argtypes = [i] * 5
+        lib.mha_ffn_forward.restype = i
+        lib.mha_ffn_forward.argtypes = [i] + [vp] * 5 + [i] * 4 + [vp, vp, sz, vp]
         lib.mha_forward_noalloc.restype = i
         lib.mha_forward_noalloc.argtypes = [i] + [vp] * 11 + [i] * 5 + [ctypes.POINTER(MaskT), vp, vp, vp]
         _lib = lib
@@ -185,6 +190,19 @@ def mha_forward_noalloc(query, key, value, w_q, b_q, w_k, b_k, w_v, b_v, w_o, b_
         _dtype_code(query), _ptr(query), _ptr(key), _ptr(value), _ptr(w_q), _ptr(b_q), _ptr(w_k),
         _ptr(b_k), _ptr(w_v), _ptr(b_v), _ptr(w_o), _ptr(b_o), B, Lq, Lk, d, h,
         ctypes.byref(mask) if mask is not None else None, _ptr(out), _ptr(p_attn), _stream(stream)))
+
+
+def ffn_workspace_size(dt: int, B: int, L: int, d_model: int, d_ff: int) -> int:
+    return int(load().mha_ffn_workspace_size(dt, B, L, d_model, d_ff))
+
+
+def mha_ffn_forward(x, w_1, b_1, w_2, b_2, *, out, workspace, stream=None):
+    """Position-wise FFN: out = max(0, x W_1^T + b_1) W_2^T + b_2 (CUDA tensors)."""
+    B, L, d = x.shape
+    d_ff = w_1.shape[0]
+    _check(load().mha_ffn_forward(
+        _dtype_code(x), _ptr(x), _ptr(w_1), _ptr(b_1), _ptr(w_2), _ptr(b_2), B, L, d, d_ff, _ptr(out),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def mha_check_device_status(reset: bool = True) -> int:

@@ -3,7 +3,8 @@
 // Computes the nn.Linear layers of MultiHeadedAttention ("003-Transformer"
 // tutorial, section "Multi-head attention": four nn.Linear(d_model, d_model)),
 // y = x W^T + b with W stored [out, in], for up to three groups per launch
-// (the Q, K and V projections). The head split of the same section
+// (the Q, K and V projections), and the two layers of the position-wise FFN
+// (same tutorial, feed-forward layer: max(0, x W_1 + b_1) W_2 + b_2). The head split of the same section
 // (view(B, L, h, d_k).transpose(1, 2)) is folded into the epilogue: each 64-wide
 // column slab of a tile is written by one TMA store straight into its head's
 // [L, d_k] plane, so no transpose kernel runs.
@@ -16,7 +17,8 @@
 //              accumulators) and issues tcgen05.mma (M=128, N=256, K=16) from
 //              one thread; tcgen05.commit frees ring stages and hands a finished
 //              accumulator to the epilogue.
-//   warps 2-5  epilogue: tcgen05.ld 64 columns at a time, add the bias, round to
+//   warps 2-5  epilogue: tcgen05.ld 64 columns at a time, add the bias (and apply
+//              ReLU for the first layer of the position-wise FFN), round to
 //              bf16, stage in swizzled shared memory (two slab buffers) and
 //              TMA-store; the accumulator is released as soon as it is read, so
 //              the next tile's MMAs overlap this tile's stores.
@@ -187,7 +189,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
                         const int cc = ch * 8 + 2 * e;
                         const float b0 = G.bias ? __bfloat162float(G.bias[n + cc]) : 0.0f;
                         const float b1 = G.bias ? __bfloat162float(G.bias[n + cc + 1]) : 0.0f;
-                        w[e] = pack_bf16x2(__uint_as_float(v[cc]) + b0, __uint_as_float(v[cc + 1]) + b1);
+                        float y0 = __uint_as_float(v[cc]) + b0;
+                        float y1 = __uint_as_float(v[cc + 1]) + b1;
+                        if (p.relu) {
+                            y0 = fmaxf(y0, 0.0f);
+                            y1 = fmaxf(y1, 0.0f);
+                        }
+                        w[e] = pack_bf16x2(y0, y1);
                     }
                     st_shared_v4(stage + ((ch ^ (row & 7)) << 4), w[0], w[1], w[2], w[3]);
                 }

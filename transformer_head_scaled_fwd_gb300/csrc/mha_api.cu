@@ -401,6 +401,86 @@ mha_status_t mha_forward(mha_dtype_t dt, const void* query, const void* key, con
     return mha_output_projection(dt, w_o, b_o, B, L_q, L_k, d_model, h, out, workspace, workspace_bytes, stream);
 }
 
+size_t mha_ffn_workspace_size(mha_dtype_t dt, int B, int L, int d_model, int d_ff) {
+    if (B <= 0 || L <= 0 || d_model <= 0 || d_ff <= 0) return 0;
+    if (dt != MHA_F32 && dt != MHA_BF16) return 0;
+    const size_t es = dt == MHA_BF16 ? 2 : 4;
+    return align256(es * B * static_cast<size_t>(L) * d_ff);
+}
+
+mha_status_t mha_ffn_forward(mha_dtype_t dt, const void* x, const void* w_1, const void* b_1, const void* w_2,
+                             const void* b_2, int B, int L, int d_model, int d_ff, void* out, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+    if (dt != MHA_F32 && dt != MHA_BF16) return fail(MHA_ERR_INVALID_ARG, "dtype %d is not MHA_F32 or MHA_BF16", dt);
+    if (B <= 0 || L <= 0 || d_model <= 0 || d_ff <= 0)
+        return fail(MHA_ERR_INVALID_ARG, "sizes must be positive (B=%d L=%d d_model=%d d_ff=%d)", B, L, d_model, d_ff);
+    if (!x || !w_1 || !w_2 || !out) return fail(MHA_ERR_INVALID_ARG, "x, W_1, W_2 and out must not be NULL");
+    if (static_cast<double>(B) * L * d_ff > 4.0e9) return fail(MHA_ERR_UNSUPPORTED, "problem too large");
+    const size_t need = mha_ffn_workspace_size(dt, B, L, d_model, d_ff);
+    if (!workspace) return fail(MHA_ERR_INVALID_ARG, "workspace is NULL");
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(MHA_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+    if (workspace_bytes < need) return fail(MHA_ERR_INVALID_ARG, "workspace too small: %zu < %zu", workspace_bytes, need);
+    const cudaStream_t s = as_stream(stream);
+    if (dt == MHA_F32) {
+        mha::F32GemmParams p{};
+        p.ngroups = 1;
+        p.B = B; p.dk = 1; p.slabs = 1; p.out_plain = 1;
+        p.g[0].L = L;
+        // layer 1: hidden = relu(x W_1^T + b_1)
+        p.K = d_model; p.N = d_ff; p.relu = 1;
+        p.g[0].A = static_cast<const float*>(x);
+        p.g[0].W = static_cast<const float*>(w_1);
+        p.g[0].bias = static_cast<const float*>(b_1);
+        p.g[0].out = static_cast<float*>(workspace);
+        cudaError_t e = mha::launch_gemm_f32(p, s);
+        if (e != cudaSuccess) return cuda_fail(e, "FFN layer 1 launch");
+        // layer 2: out = hidden W_2^T + b_2
+        p.K = d_ff; p.N = d_model; p.relu = 0;
+        p.g[0].A = static_cast<const float*>(workspace);
+        p.g[0].W = static_cast<const float*>(w_2);
+        p.g[0].bias = static_cast<const float*>(b_2);
+        p.g[0].out = static_cast<float*>(out);
+        e = mha::launch_gemm_f32(p, s);
+        if (e != cudaSuccess) return cuda_fail(e, "FFN layer 2 launch");
+        return MHA_OK;
+    }
+    if (d_model % 64 != 0 || d_ff % 64 != 0)
+        return fail(MHA_ERR_UNSUPPORTED, "bf16 FFN needs d_model and d_ff multiples of 64 (got %d, %d)", d_model, d_ff);
+    const void* ptrs[6] = {x, w_1, b_1, w_2, b_2, out};
+    for (const void* ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return fail(MHA_ERR_INVALID_ARG, "bf16 tensors must be 16-byte aligned");
+    mha_status_t st = get_encoder();
+    if (st != MHA_OK) return st;
+    int* status = device_status_ptr();
+    if (!status) return fail(MHA_ERR_CUDA, "device status word unavailable");
+    const int tiles_per_b = (L + mha::kGemmBM - 1) / mha::kGemmBM;
+    for (int layer = 0; layer < 2; ++layer) {
+        mha::GemmParams p;
+        memset(&p, 0, sizeof(p));
+        const int K = layer == 0 ? d_model : d_ff;
+        const int N = layer == 0 ? d_ff : d_model;
+        const void* A = layer == 0 ? x : workspace;
+        void* O = layer == 0 ? workspace : out;
+        if ((st = map_rows(&p.a[0], A, B, L, K, "FFN input")) != MHA_OK) return st;
+        if ((st = map_weight(&p.w[0], layer == 0 ? w_1 : w_2, N, K)) != MHA_OK) return st;
+        if ((st = map_rows(&p.out[0], O, B, L, N, "FFN output")) != MHA_OK) return st;
+        p.g[0].L = L;
+        p.g[0].tiles_per_b = tiles_per_b;
+        p.g[0].m_tiles = B * tiles_per_b;
+        p.g[0].bias = static_cast<const __nv_bfloat16*>(layer == 0 ? b_1 : b_2);
+        p.ngroups = 1;
+        p.K = K;
+        p.N = N;
+        p.out_plain = 1;
+        p.relu = layer == 0;
+        p.status = status;
+        cudaError_t e = mha::launch_gemm_tc(p, p.g[0].m_tiles, s);
+        if (e != cudaSuccess) return cuda_fail(e, layer == 0 ? "FFN layer 1 launch" : "FFN layer 2 launch");
+    }
+    return MHA_OK;
+}
+
 size_t mha_host_staging_size(mha_dtype_t dt, int B, int L_q, int L_k, int d_model, int kv_distinct,
                              int q_distinct) {
     if (B <= 0 || L_q <= 0 || L_k <= 0 || d_model <= 0) return 0;

@@ -41,6 +41,7 @@ struct GemmParams {
     int K;
     int N;
     int out_plain;        // 1: plain [B, L, N] output
+    int relu;             // 1: max(0, .) after the bias (first FFN layer)
     int* status;
 };
 
@@ -103,6 +104,7 @@ struct F32GemmParams {
     int dk;
     int slabs;           // slabs per batch item in a head-split output
     int out_plain;
+    int relu;            // 1: max(0, .) after the bias
 };
 cudaError_t launch_gemm_f32(const F32GemmParams& p, cudaStream_t s);
 

@@ -66,7 +66,8 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(const F32GemmParams p) {
         for (int j = 0; j < 4; ++j) {
             const int n = n0 + tx * 4 + j;
             if (n >= p.N) continue;
-            const float y = acc[i][j] + (G.bias ? G.bias[n] : 0.0f);
+            float y = acc[i][j] + (G.bias ? G.bias[n] : 0.0f);
+            if (p.relu) y = fmaxf(y, 0.0f);
             if (p.out_plain) {
                 G.out[m * p.N + n] = y;
             } else {

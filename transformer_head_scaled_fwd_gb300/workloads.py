@@ -170,3 +170,36 @@ def sample_rows(L: int, n: int, seed: int) -> np.ndarray:
     inner = rng.choice(np.arange(1, L - 1), size=max(0, n - 2), replace=False) if L > 2 else []
     rows = sorted(set([0, L - 1]) | set(int(x) for x in inner))
     return np.asarray(rows, dtype=np.int32)
+
+
+@dataclass
+class FFNInputs:
+    x: np.ndarray
+    w_1: np.ndarray
+    b_1: np.ndarray
+    w_2: np.ndarray
+    b_2: np.ndarray
+    dtype: str
+
+
+FFN_WORKLOADS = {
+    # the pages' base sizes: d_model 512, d_ff 2048 ("003-Transformer", make_model)
+    "ffn_base": dict(B=32, L=256, d_model=512, d_ff=2048),
+    # the long workload's width with the same 4x expansion
+    "ffn_long": dict(B=4, L=8192, d_model=1024, d_ff=4096),
+}
+
+
+def make_ffn_inputs(B: int, L: int, d_model: int, d_ff: int, *, seed: int = 0, dtype: str = "bf16",
+                    bias_scale: float = 0.1) -> FFNInputs:
+    """x ~ N(0, 1); W_1 [d_ff, d_model], W_2 [d_model, d_ff] Xavier-uniform; biases U(-s, s)."""
+    g = torch.Generator().manual_seed(SEED_BASE + 104729 * (seed + 1))
+    x = torch.randn((B, L, d_model), generator=g)
+    w1 = xavier_uniform(g, d_ff, d_model)
+    b1 = (torch.rand((d_ff,), generator=g) * 2 - 1) * bias_scale
+    w2 = xavier_uniform(g, d_model, d_ff)
+    b2 = (torch.rand((d_model,), generator=g) * 2 - 1) * bias_scale
+    ts = [x, w1, b1, w2, b2]
+    if dtype == "bf16":
+        ts = [round_bf16(t) for t in ts]
+    return FFNInputs(*[t.contiguous().numpy() for t in ts], dtype)
