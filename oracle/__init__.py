@@ -66,6 +66,9 @@ def _load():
                                           ctypes.c_int, dp]
             lib.oracle_ffn_forward.restype = ctypes.c_int
             lib.oracle_ffn_forward.argtypes = [dp] * 5 + [ctypes.c_long, ctypes.c_int, ctypes.c_int, dp]
+            lib.oracle_layernorm.restype = ctypes.c_int
+            lib.oracle_layernorm.argtypes = [dp] * 3 + [ctypes.c_long, ctypes.c_int, ctypes.c_double,
+                                                        ctypes.c_int, dp]
             lib.oracle_num_threads.restype = ctypes.c_int
             lib.oracle_num_threads.argtypes = []
             _lib = lib
@@ -157,3 +160,34 @@ def ffn_forward(x, w_1, b_1, w_2, b_2):
     if rc != 0:
         raise ValueError(f"oracle_ffn_forward rejected its arguments (code {rc})")
     return out
+
+
+LN_ANNOTATED, LN_TORCH = 0, 1
+
+
+def layernorm(x, a=None, b=None, eps=1e-6, kind=LN_ANNOTATED):
+    """Row LayerNorm in fp64. kind 0: a (x - mean) / (std_unbiased + eps) + b ("The Annotated
+    Transformer"); kind 1: nn.LayerNorm, a (x - mean) / sqrt(var_biased + eps) + b."""
+    lib = _load()
+    x = _f64(x)
+    a, b = _f64(a), _f64(b)
+    d = x.shape[-1]
+    y = np.empty_like(x)
+    rc = lib.oracle_layernorm(_ptr(x, ctypes.c_double), _ptr(a, ctypes.c_double), _ptr(b, ctypes.c_double),
+                              int(np.prod(x.shape[:-1])), d, float(eps), int(kind), _ptr(y, ctypes.c_double))
+    if rc != 0:
+        raise ValueError(f"oracle_layernorm rejected its arguments (code {rc})")
+    return y
+
+
+def sublayer_forward(x, ln_a, ln_b, eps, kind, w_q, b_q, w_k, b_k, w_v, b_v, w_o, b_o, h, memory=None,
+                     causal=False, valid_lens=None, dense=None, rows=None):
+    """The residual sublayer around multi-head attention ("The Annotated Transformer",
+    SublayerConnection.forward): x + sublayer(norm(x)) with sublayer = self_attn(y, y, y, mask)
+    when memory is None, else src_attn(y, memory, memory, mask); dropout is the identity."""
+    y = layernorm(x, ln_a, ln_b, eps, kind)
+    kv = y if memory is None else _f64(memory)
+    att = mha_forward(y, kv, kv, w_q, b_q, w_k, b_k, w_v, b_v, w_o, b_o, h, causal=causal,
+                      valid_lens=valid_lens, dense=dense, rows=rows)
+    xs = _f64(x) if rows is None else _f64(x)[:, rows]
+    return xs + att

@@ -205,3 +205,32 @@ int oracle_ffn_forward(const double* x, const double* w_1, const double* b_1,
     free(hid);
     return 0;
 }
+
+/*
+ * oracle_layernorm -- per row of x [rows, d] in fp64.
+ * kind 0 ("The Annotated Transformer", LayerNorm):
+ *     a * (x - mean) / (std + eps) + b,  std = sqrt(sum (x - mean)^2 / (d - 1))  (unbiased)
+ * kind 1 (nn.LayerNorm, "003-Transformer" SublayerConnection):
+ *     a * (x - mean) / sqrt(var + eps) + b,  var = sum (x - mean)^2 / d  (biased)
+ * a, b [d] or NULL (= ones / zeros). Returns 0, or 1 on bad sizes / kind.
+ */
+int oracle_layernorm(const double* x, const double* a, const double* b, long rows, int d, double eps,
+                     int kind, double* y)
+{
+    if (rows <= 0 || d <= 0 || (kind != 0 && kind != 1) || (kind == 0 && d < 2)) return 1;
+    long r;
+#pragma omp parallel for schedule(static)
+    for (r = 0; r < rows; ++r) {
+        const double* xr = x + r * (long)d;
+        double* yr = y + r * (long)d;
+        double mean = 0.0;
+        for (int i = 0; i < d; ++i) mean += xr[i];
+        mean /= d;
+        double ss = 0.0;
+        for (int i = 0; i < d; ++i) ss += (xr[i] - mean) * (xr[i] - mean);
+        const double denom = (kind == 0) ? sqrt(ss / (d - 1)) + eps : sqrt(ss / d + eps);
+        for (int i = 0; i < d; ++i)
+            yr[i] = (a ? a[i] : 1.0) * (xr[i] - mean) / denom + (b ? b[i] : 0.0);
+    }
+    return 0;
+}
