@@ -449,6 +449,64 @@ def run_gpu_ffn(args):
     print(json.dumps(line), flush=True)
 
 
+def run_gpu_sublayer(args):
+    """Pre-norm residual sublayer x + MHA(LayerNorm(x)) on the long workload: TFLOP/s counts the
+    attention sublayer's algorithmic flops (LayerNorm and the residual add are HBM-bound extras)."""
+    import torch
+
+    from transformer_head_scaled_fwd_gb300 import binding
+    from transformer_head_scaled_fwd_gb300 import build as B
+    from transformer_head_scaled_fwd_gb300 import workloads as W
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    B.build()
+    binding.load()
+    peaks, peak_src = load_peaks()
+    wl = W.WORKLOADS[args.workload]
+    inp = rank_inputs(wl, rank)
+    ln = W.make_ln_params(wl.d_model, seed=rank)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda().to(torch.bfloat16)
+    x = dev(inp.query)
+    Wt = [dev(inp.weights[n]) for n in ("w_q", "b_q", "w_k", "b_k", "w_v", "b_v", "w_o", "b_o")]
+    g, bb = dev(ln[0]), dev(ln[1])
+    Bn, L, d = x.shape
+    vl = None if inp.valid_lens is None else torch.from_numpy(inp.valid_lens).cuda()
+    mask = binding.make_mask(wl.causal, vl, None)
+    ws = torch.empty(binding.sublayer_workspace_size(binding.MHA_BF16, Bn, L, 0, d, wl.h), dtype=torch.uint8,
+                     device="cuda")
+    out = torch.empty_like(x)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    proj, attn = algorithmic_flops(Bn, L, L, d, wl.h, wl.causal, inp.valid_lens)
+    K, Wm = args.steps, args.warmup
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K + Wm)]
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        for s_ in range(Wm + K):
+            flush.zero_()
+            evs[s_][0].record(stream)
+            binding.mha_sublayer_forward(x, g, bb, 1e-6, 0, *Wt, wl.h, out=out, workspace=ws, mask=mask,
+                                         stream=stream)
+            evs[s_][1].record(stream)
+        torch.cuda.synchronize()
+    if binding.mha_check_device_status(reset=True) != 0:
+        raise RuntimeError("a pipeline wait gave up inside a kernel")
+    ms = sum(a.elapsed_time(b) for a, b in evs[Wm:]) / K
+    value = (proj + attn) / (ms * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    line = {
+        "metric": "pre-norm residual MHA sublayer fwd TFLOP/s (bf16)", "value": value, "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": K, "warmup": Wm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded)",
+        "config": {"workload": "x + MHA(LayerNorm(x)): " + DESCRIPTION[args.workload],
+                   "layernorm": "unbiased std + eps 1e-6", "l2": "flushed before every step"},
+        "tokens_per_s": Bn * L / (ms * 1e-3), "pct_of_bf16_peak": 100 * value / peak,
+        "gpu_launches": 4 * K, "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -458,8 +516,9 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD, choices=["enc", "dec", "xattn", "long"])
     ap.add_argument("--ref-prefix", type=int, default=2048, help="causal prefix length of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--path", choices=["mha", "ffn"], default="mha",
-                    help="mha: the attention sublayer (default); ffn: the position-wise FFN")
+    ap.add_argument("--path", choices=["mha", "ffn", "sublayer"], default="mha",
+                    help="mha: the attention sublayer (default); ffn: the position-wise FFN; "
+                         "sublayer: x + MHA(LayerNorm(x))")
     ap.add_argument("--ffn-workload", default="ffn_long", choices=["ffn_base", "ffn_long"])
     args = ap.parse_args()
     if args.warmup < 3 and args.impl != "reference":
@@ -468,6 +527,8 @@ def main():
         run_reference(args)
     elif args.path == "ffn":
         run_gpu_ffn(args)
+    elif args.path == "sublayer":
+        run_gpu_sublayer(args)
     else:
         run_gpu(args)
 

@@ -199,6 +199,36 @@ mha_status_t mha_forward_noalloc(mha_dtype_t dt,
                                  void* stream);
 
 /*
+ * The residual sublayer around multi-head attention, pre-norm form
+ * ("The Annotated Transformer", SublayerConnection: x + dropout(sublayer(norm(x))),
+ * dropout = identity):
+ *   y   = LayerNorm(x)
+ *   out = x + MultiHeadedAttention(y, y, y, mask)              if memory == NULL (self-attention)
+ *   out = x + MultiHeadedAttention(y, memory, memory, mask)    otherwise (source attention,
+ *         "The Annotated Transformer", DecoderLayer: src_attn(x, m, m, src_mask))
+ * LayerNorm over the last dimension, ln_kind selects the pages' two forms:
+ *   0  a (x - mean) / (std + eps) + b, std unbiased ("The Annotated Transformer", LayerNorm, eps 1e-6)
+ *   1  a (x - mean) / sqrt(var + eps) + b, var biased (nn.LayerNorm, "003-Transformer")
+ *   ln_gain / ln_bias [d_model] or NULL (ones / zeros), type dt.
+ * x [B, L, d_model]; memory [B, L_mem, d_model] or NULL; out [B, L, d_model] (may alias x: each
+ * element of x is read by the thread that then writes the same element of out).
+ * d_model <= 2048. Workspace >= mha_sublayer_workspace_size(...): LayerNorm(x) followed by the
+ * workspace of mha_forward. Launches: LayerNorm, the three stages of mha_forward, with the
+ * residual added in the W_o epilogue.
+ */
+size_t mha_sublayer_workspace_size(mha_dtype_t dt, int B, int L, int L_mem, int d_model, int h);
+mha_status_t mha_sublayer_forward(mha_dtype_t dt, const void* x, const void* memory,
+                                  const void* ln_gain, const void* ln_bias, float ln_eps, int ln_kind,
+                                  const void* w_q, const void* b_q,
+                                  const void* w_k, const void* b_k,
+                                  const void* w_v, const void* b_v,
+                                  const void* w_o, const void* b_o,
+                                  int B, int L, int L_mem, int d_model, int h,
+                                  const mha_mask_t* mask,
+                                  void* out, void* workspace, size_t workspace_bytes,
+                                  void* stream);
+
+/*
  * Position-wise feed-forward network ("003-Transformer" tutorial, feed-forward
  * layer; "From RNN to Attention", part 3, FFN):
  *   out = max(0, x W_1^T + b_1) W_2^T + b_2        (dropout = identity)

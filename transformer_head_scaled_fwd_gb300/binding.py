@@ -25,7 +25,7 @@ MHA_F32, MHA_BF16 = 0, 1
 EXPORTS = ("mha_workspace_size", "mha_forward", "mha_qkv_projection", "mha_attention_core",
            "mha_output_projection", "mha_host_staging_size", "mha_forward_host", "mha_last_error",
            "mha_check_device_status", "mha_version", "mha_forward_noalloc", "mha_ffn_workspace_size",
-           "mha_ffn_forward")
+           "mha_ffn_forward", "mha_sublayer_workspace_size", "mha_sublayer_forward")
 
 
 class MHAError(RuntimeError):
@@ -79,6 +79,11 @@ def load(path: str | None = None):
         lib.mha_ffn_workspace_size.argtypes = [i] * 5
         lib.mha_ffn_forward.restype = i
         lib.mha_ffn_forward.argtypes = [i] + [vp] * 5 + [i] * 4 + [vp, vp, sz, vp]
+        lib.mha_sublayer_workspace_size.restype = sz
+        lib.mha_sublayer_workspace_size.argtypes = [i] * 6
+        lib.mha_sublayer_forward.restype = i
+        lib.mha_sublayer_forward.argtypes = ([i, vp, vp, vp, vp, ctypes.c_float, i] + [vp] * 8 + [i] * 5
+                                             + [ctypes.POINTER(MaskT), vp, vp, sz, vp])
         lib.mha_forward_noalloc.restype = i
         lib.mha_forward_noalloc.argtypes = [i] + [vp] * 11 + [i] * 5 + [ctypes.POINTER(MaskT), vp, vp, vp]
         _lib = lib
@@ -190,6 +195,25 @@ def mha_forward_noalloc(query, key, value, w_q, b_q, w_k, b_k, w_v, b_v, w_o, b_
         _dtype_code(query), _ptr(query), _ptr(key), _ptr(value), _ptr(w_q), _ptr(b_q), _ptr(w_k),
         _ptr(b_k), _ptr(w_v), _ptr(b_v), _ptr(w_o), _ptr(b_o), B, Lq, Lk, d, h,
         ctypes.byref(mask) if mask is not None else None, _ptr(out), _ptr(p_attn), _stream(stream)))
+
+
+LN_UNBIASED_STD, LN_TORCH = 0, 1
+
+
+def sublayer_workspace_size(dt: int, B: int, L: int, L_mem: int, d_model: int, h: int) -> int:
+    return int(load().mha_sublayer_workspace_size(dt, B, L, L_mem, d_model, h))
+
+
+def mha_sublayer_forward(x, ln_gain, ln_bias, ln_eps, ln_kind, w_q, b_q, w_k, b_k, w_v, b_v, w_o, b_o, h, *,
+                         out, workspace, memory=None, mask=None, stream=None):
+    """out = x + MHA(LayerNorm(x), kv, kv, mask), kv = LayerNorm(x) or memory (CUDA tensors)."""
+    B, L, d = x.shape
+    L_mem = memory.shape[1] if memory is not None else 0
+    _check(load().mha_sublayer_forward(
+        _dtype_code(x), _ptr(x), _ptr(memory), _ptr(ln_gain), _ptr(ln_bias), float(ln_eps), int(ln_kind),
+        _ptr(w_q), _ptr(b_q), _ptr(w_k), _ptr(b_k), _ptr(w_v), _ptr(b_v), _ptr(w_o), _ptr(b_o), B, L, L_mem, d, h,
+        ctypes.byref(mask) if mask is not None else None, _ptr(out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def ffn_workspace_size(dt: int, B: int, L: int, d_model: int, d_ff: int) -> int:

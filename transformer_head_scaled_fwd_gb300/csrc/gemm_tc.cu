@@ -18,7 +18,8 @@
 //              one thread; tcgen05.commit frees ring stages and hands a finished
 //              accumulator to the epilogue.
 //   warps 2-5  epilogue: tcgen05.ld 64 columns at a time, add the bias (and apply
-//              ReLU for the first layer of the position-wise FFN), round to
+//              ReLU for the first layer of the position-wise FFN, or the
+//              residual of the sublayer connection for W_o), round to
 //              bf16, stage in swizzled shared memory (two slab buffers) and
 //              TMA-store; the accumulator is released as soon as it is read, so
 //              the next tile's MMAs overlap this tile's stores.
@@ -181,9 +182,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
                 if (issuer && slabs_issued >= 2) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
                 named_bar_sync(1, 128);
                 const uint32_t stage = smem_u32(base + kOffStage + sb * kSlabBytes) + row * 128;
+                const bool has_res = G.residual != nullptr && c.l0 + row < G.L;
+                const __nv_bfloat16* res_row =
+                    has_res ? G.residual + (static_cast<long>(c.b) * G.L + c.l0 + row) * p.N + n : nullptr;
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
                     uint32_t w[4];
+                    uint4 rv = make_uint4(0, 0, 0, 0);
+                    if (has_res) rv = *reinterpret_cast<const uint4*>(res_row + ch * 8);
+                    const __nv_bfloat162* r2 = reinterpret_cast<const __nv_bfloat162*>(&rv);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int cc = ch * 8 + 2 * e;
@@ -194,6 +201,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
                         if (p.relu) {
                             y0 = fmaxf(y0, 0.0f);
                             y1 = fmaxf(y1, 0.0f);
+                        }
+                        if (has_res) {   // residual connection: x + sublayer(...)
+                            const float2 rf = __bfloat1622float2(r2[e]);
+                            y0 += rf.x;
+                            y1 += rf.y;
                         }
                         w[e] = pack_bf16x2(y0, y1);
                     }

@@ -327,17 +327,14 @@ mha_status_t mha_attention_core(mha_dtype_t dt, int B, int L_q, int L_k, int d_m
     return MHA_OK;
 }
 
-mha_status_t mha_output_projection(mha_dtype_t dt, const void* w_o, const void* b_o, int B, int L_q, int L_k,
-                                   int d_model, int h, void* out, void* workspace, size_t workspace_bytes,
-                                   void* stream) {
-    mha_status_t st = check_sizes(dt, B, L_q, L_k, d_model, h);
-    if (st != MHA_OK) return st;
-    if (!w_o || !out) return fail(MHA_ERR_INVALID_ARG, "W_o and out must not be NULL");
-    Layout L;
-    if ((st = check_workspace(dt, B, L_q, L_k, d_model, h, workspace, workspace_bytes, &L)) != MHA_OK) return st;
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    const cudaStream_t s = as_stream(stream);
+}  // extern "C"
 
+namespace {
+
+// out = ctx W_o^T + b_o (+ residual), reading ctx from the workspace; no argument checks.
+mha_status_t output_projection_impl(mha_dtype_t dt, const void* w_o, const void* b_o, const void* residual,
+                                    int B, int L_q, int d_model, int h, void* out, const Layout& L, uint8_t* ws,
+                                    cudaStream_t s) {
     if (dt == MHA_F32) {
         mha::F32GemmParams p{};
         p.ngroups = 1;
@@ -345,15 +342,15 @@ mha_status_t mha_output_projection(mha_dtype_t dt, const void* w_o, const void* 
         p.g[0].A = reinterpret_cast<const float*>(ws + L.ctx);
         p.g[0].W = static_cast<const float*>(w_o);
         p.g[0].bias = static_cast<const float*>(b_o);
+        p.g[0].residual = static_cast<const float*>(residual);
         p.g[0].out = static_cast<float*>(out);
         p.g[0].L = L_q;
         cudaError_t e = mha::launch_gemm_f32(p, s);
         if (e != cudaSuccess) return cuda_fail(e, "fp32 output projection launch");
         return MHA_OK;
     }
-    if (!aligned16(w_o) || !aligned16(out) || (b_o && !aligned16(b_o)))
-        return fail(MHA_ERR_INVALID_ARG, "bf16 tensors must be 16-byte aligned");
-    if ((st = get_encoder()) != MHA_OK) return st;
+    mha_status_t st = get_encoder();
+    if (st != MHA_OK) return st;
     mha::GemmParams p;
     memset(&p, 0, sizeof(p));
     if ((st = map_rows(&p.a[0], ws + L.ctx, B, L_q, d_model, "context")) != MHA_OK) return st;
@@ -363,6 +360,7 @@ mha_status_t mha_output_projection(mha_dtype_t dt, const void* w_o, const void* 
     p.g[0].tiles_per_b = (L_q + mha::kGemmBM - 1) / mha::kGemmBM;
     p.g[0].m_tiles = B * p.g[0].tiles_per_b;
     p.g[0].bias = static_cast<const __nv_bfloat16*>(b_o);
+    p.g[0].residual = static_cast<const __nv_bfloat16*>(residual);
     p.ngroups = 1;
     p.K = d_model;
     p.N = d_model;
@@ -372,6 +370,24 @@ mha_status_t mha_output_projection(mha_dtype_t dt, const void* w_o, const void* 
     cudaError_t e = mha::launch_gemm_tc(p, p.g[0].m_tiles, s);
     if (e != cudaSuccess) return cuda_fail(e, "output projection launch");
     return MHA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mha_status_t mha_output_projection(mha_dtype_t dt, const void* w_o, const void* b_o, int B, int L_q, int L_k,
+                                   int d_model, int h, void* out, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
+    mha_status_t st = check_sizes(dt, B, L_q, L_k, d_model, h);
+    if (st != MHA_OK) return st;
+    if (!w_o || !out) return fail(MHA_ERR_INVALID_ARG, "W_o and out must not be NULL");
+    Layout L;
+    if ((st = check_workspace(dt, B, L_q, L_k, d_model, h, workspace, workspace_bytes, &L)) != MHA_OK) return st;
+    if (dt == MHA_BF16 && (!aligned16(w_o) || !aligned16(out) || (b_o && !aligned16(b_o))))
+        return fail(MHA_ERR_INVALID_ARG, "bf16 tensors must be 16-byte aligned");
+    return output_projection_impl(dt, w_o, b_o, nullptr, B, L_q, d_model, h, out, L,
+                                  static_cast<uint8_t*>(workspace), as_stream(stream));
 }
 
 mha_status_t mha_forward(mha_dtype_t dt, const void* query, const void* key, const void* value, const void* w_q,
@@ -399,6 +415,65 @@ mha_status_t mha_forward(mha_dtype_t dt, const void* query, const void* key, con
         MHA_OK)
         return st;
     return mha_output_projection(dt, w_o, b_o, B, L_q, L_k, d_model, h, out, workspace, workspace_bytes, stream);
+}
+
+size_t mha_sublayer_workspace_size(mha_dtype_t dt, int B, int L, int L_mem, int d_model, int h) {
+    const size_t ws = mha_workspace_size(dt, B, L, L_mem > 0 ? L_mem : L, d_model, h);
+    if (ws == 0) return 0;
+    const size_t es = dt == MHA_BF16 ? 2 : 4;
+    return align256(es * B * static_cast<size_t>(L) * d_model) + ws;
+}
+
+mha_status_t mha_sublayer_forward(mha_dtype_t dt, const void* x, const void* memory, const void* ln_gain,
+                                  const void* ln_bias, float ln_eps, int ln_kind, const void* w_q, const void* b_q,
+                                  const void* w_k, const void* b_k, const void* w_v, const void* b_v,
+                                  const void* w_o, const void* b_o, int B, int L, int L_mem, int d_model, int h,
+                                  const mha_mask_t* mask, void* out, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+    const int Lk = memory ? L_mem : L;
+    mha_status_t st = check_sizes(dt, B, L, Lk, d_model, h);
+    if (st != MHA_OK) return st;
+    if ((st = check_mask(mask, L, Lk)) != MHA_OK) return st;
+    if (!x || !w_q || !w_k || !w_v || !w_o || !out)
+        return fail(MHA_ERR_INVALID_ARG, "x, W_q, W_k, W_v, W_o and out must not be NULL");
+    if (ln_kind != 0 && ln_kind != 1) return fail(MHA_ERR_INVALID_ARG, "ln_kind must be 0 or 1 (got %d)", ln_kind);
+    if (ln_kind == 0 && d_model < 2) return fail(MHA_ERR_INVALID_ARG, "unbiased std needs d_model >= 2");
+    if (!(ln_eps >= 0.0f)) return fail(MHA_ERR_INVALID_ARG, "ln_eps must be >= 0");
+    if (d_model > mha::layernorm_max_d())
+        return fail(MHA_ERR_UNSUPPORTED, "LayerNorm implements d_model <= %d", mha::layernorm_max_d());
+    const size_t need = mha_sublayer_workspace_size(dt, B, L, Lk, d_model, h);
+    if (!workspace) return fail(MHA_ERR_INVALID_ARG, "workspace is NULL");
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(MHA_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+    if (workspace_bytes < need) return fail(MHA_ERR_INVALID_ARG, "workspace too small: %zu < %zu", workspace_bytes, need);
+    if (dt == MHA_BF16) {
+        const void* ptrs[14] = {x, memory, ln_gain, ln_bias, w_q, b_q, w_k, b_k, w_v, b_v, w_o, b_o, out, workspace};
+        for (const void* ptr : ptrs)
+            if (ptr && !aligned16(ptr)) return fail(MHA_ERR_INVALID_ARG, "bf16 tensors must be 16-byte aligned");
+    }
+    const size_t es = dt == MHA_BF16 ? 2 : 4;
+    uint8_t* y = static_cast<uint8_t*>(workspace);
+    uint8_t* mws = y + align256(es * B * static_cast<size_t>(L) * d_model);
+    const size_t mws_bytes = workspace_bytes - (mws - y);
+    const cudaStream_t s = as_stream(stream);
+    // 1. y = LayerNorm(x)
+    mha::LayerNormParams ln{};
+    ln.x = x; ln.y = y; ln.gain = ln_gain; ln.bias = ln_bias;
+    ln.rows = static_cast<long>(B) * L; ln.d = d_model; ln.eps = ln_eps; ln.kind = ln_kind;
+    ln.bf16 = dt == MHA_BF16;
+    cudaError_t e = mha::launch_layernorm(ln, s);
+    if (e != cudaSuccess) return cuda_fail(e, "LayerNorm launch");
+    // 2. attention sublayer on y (self) or on (y, memory, memory) (source attention)
+    const void* kv = memory ? memory : y;
+    if ((st = mha_qkv_projection(dt, y, kv, kv, w_q, b_q, w_k, b_k, w_v, b_v, B, L, Lk, d_model, h, mws, mws_bytes,
+                                 stream)) != MHA_OK)
+        return st;
+    if ((st = mha_attention_core(dt, B, L, Lk, d_model, h, mask, nullptr, mws, mws_bytes, stream)) != MHA_OK)
+        return st;
+    // 3. out = x + (ctx W_o^T + b_o): the residual is added in the W_o epilogue
+    Layout Lo;
+    layout_of(dt, B, L, Lk, d_model, h, &Lo);
+    return output_projection_impl(dt, w_o, b_o, x, B, L, d_model, h, out, Lo, mws, s);
 }
 
 size_t mha_ffn_workspace_size(mha_dtype_t dt, int B, int L, int d_model, int d_ff) {

@@ -29,7 +29,8 @@ struct GemmGroup {
     int tiles_per_b;   // ceil(L / 128)
     int m_tiles;       // B * tiles_per_b
     int out_j0;        // first 64-column slab of this group in a head-split output
-    const __nv_bfloat16* bias;   // [N] or nullptr
+    const __nv_bfloat16* bias;       // [N] or nullptr
+    const __nv_bfloat16* residual;   // plain output only: [B, L, N] added after the bias, or nullptr
 };
 
 struct GemmParams {
@@ -93,6 +94,7 @@ struct F32GemmGroup {
     const float* A;      // [B, L, K]
     const float* W;      // [N, K]
     const float* bias;   // [N] or nullptr
+    const float* residual;   // plain output only: [B, L, N] added after the bias, or nullptr
     float* out;          // head-split [B, slabs, L, dk] or plain [B, L, N]
     int L;
     int out_j0;
@@ -120,5 +122,20 @@ struct F32AttnParams {
     int dense_mq;
 };
 cudaError_t launch_attn_f32(const F32AttnParams& p, cudaStream_t s);
+
+// ------------------------------------------------------------ LayerNorm (rows of length d)
+struct LayerNormParams {
+    const void* x;       // [rows, d]
+    void* y;             // [rows, d]
+    const void* gain;    // [d] or nullptr (ones)
+    const void* bias;    // [d] or nullptr (zeros)
+    long rows;
+    int d;
+    float eps;
+    int kind;            // 0: unbiased std + eps ("The Annotated Transformer"); 1: nn.LayerNorm
+    int bf16;            // element type: 1 bf16, 0 fp32
+};
+int layernorm_max_d();
+cudaError_t launch_layernorm(const LayerNormParams& p, cudaStream_t s);
 
 }  // namespace mha

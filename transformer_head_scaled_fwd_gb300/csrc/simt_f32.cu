@@ -68,6 +68,7 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(const F32GemmParams p) {
             if (n >= p.N) continue;
             float y = acc[i][j] + (G.bias ? G.bias[n] : 0.0f);
             if (p.relu) y = fmaxf(y, 0.0f);
+            if (G.residual) y += G.residual[m * p.N + n];
             if (p.out_plain) {
                 G.out[m * p.N + n] = y;
             } else {

@@ -203,3 +203,13 @@ def make_ffn_inputs(B: int, L: int, d_model: int, d_ff: int, *, seed: int = 0, d
     if dtype == "bf16":
         ts = [round_bf16(t) for t in ts]
     return FFNInputs(*[t.contiguous().numpy() for t in ts], dtype)
+
+
+def make_ln_params(d_model: int, *, seed: int = 0, dtype: str = "bf16"):
+    """LayerNorm gain U(0.5, 1.5) and bias U(-0.1, 0.1), seeded (numpy fp32, bf16-exact for bf16)."""
+    g = torch.Generator().manual_seed(SEED_BASE + 15485863 * (seed + 1))
+    a = torch.rand((d_model,), generator=g) + 0.5
+    b = (torch.rand((d_model,), generator=g) * 2 - 1) * 0.1
+    if dtype == "bf16":
+        a, b = round_bf16(a), round_bf16(b)
+    return a.contiguous().numpy(), b.contiguous().numpy()
