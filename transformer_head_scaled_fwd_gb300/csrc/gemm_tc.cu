@@ -162,6 +162,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
             const TileCoord c = tile_coord(p, tile, n_tiles);
             const GemmGroup& G = p.g[c.grp];
             const int acc = use & 1;
+            if (G.residual != nullptr && c.l0 + row < G.L) {
+                // pull this row's residual (BN bf16 = 4 lines of 128 B) towards L2 while the MMAs run
+                const char* rp = reinterpret_cast<const char*>(
+                    G.residual + (static_cast<long>(c.b) * G.L + c.l0 + row) * p.N + c.n0);
+                const int lines = min(BN, p.N - c.n0) / 64;
+                for (int q = 0; q < lines; ++q) asm volatile("prefetch.global.L2 [%0];" ::"l"(rp + q * 128));
+            }
             mbar_wait(&sm->acc_full[acc], (use >> 1) & 1, abort_flag, p.status, 0x103);
             __syncwarp();
             tc_fence_after();
