@@ -229,6 +229,38 @@ mha_status_t mha_sublayer_forward(mha_dtype_t dt, const void* x, const void* mem
                                   void* stream);
 
 /*
+ * Incremental decoding with a key/value cache (bf16, d_k = 64).
+ * At prediction time the d2l Transformer decoder (d2l Transformer chapter, DecoderBlock:
+ * state[2] keeps the representations decoded so far and torch.cat appends the new one as
+ * keys and values) attends from the newest token to every token so far, itself included.
+ * This library caches the PROJECTED keys and values, which gives the same result.
+ *   k_cache, v_cache  device [B, h, L_max, 64] bf16: position t of sequence b, head i.
+ *   mha_kv_cache_prefill: projects x [B, T, d_model] into positions 0..T-1 of both caches
+ *     (K = x W_k^T + b_k, V = x W_v^T + b_v); T <= L_max.
+ *   mha_decode_step: one new token per sequence, x_new [B, d_model]:
+ *     q, k, v = x_new W^T + b; k, v written at position cache_len[b] (device int32 [B]),
+ *     which the step then increments on the device; out [B, d_model] = the sublayer's output
+ *     for the new token: attention of q over the cache_len[b] + 1 cached positions (no mask
+ *     needed), concat, W_o. A sequence whose cache is full (cache_len[b] >= L_max) appends
+ *     nothing and the step records code 0x301 in the device status word
+ *     (mha_check_device_status). Workspace >= mha_decode_workspace_size(...), 256-byte aligned.
+ */
+size_t mha_decode_workspace_size(int B, int d_model, int h, int L_max);
+mha_status_t mha_kv_cache_prefill(mha_dtype_t dt, const void* x,
+                                  const void* w_k, const void* b_k,
+                                  const void* w_v, const void* b_v,
+                                  int B, int T, int d_model, int h,
+                                  void* k_cache, void* v_cache, int L_max, void* stream);
+mha_status_t mha_decode_step(mha_dtype_t dt, const void* x_new,
+                             const void* w_q, const void* b_q,
+                             const void* w_k, const void* b_k,
+                             const void* w_v, const void* b_v,
+                             const void* w_o, const void* b_o,
+                             int B, int d_model, int h,
+                             void* k_cache, void* v_cache, int32_t* cache_len, int L_max,
+                             void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Position-wise feed-forward network ("003-Transformer" tutorial, feed-forward
  * layer; "From RNN to Attention", part 3, FFN):
  *   out = max(0, x W_1^T + b_1) W_2^T + b_2        (dropout = identity)

@@ -25,7 +25,8 @@ MHA_F32, MHA_BF16 = 0, 1
 EXPORTS = ("mha_workspace_size", "mha_forward", "mha_qkv_projection", "mha_attention_core",
            "mha_output_projection", "mha_host_staging_size", "mha_forward_host", "mha_last_error",
            "mha_check_device_status", "mha_version", "mha_forward_noalloc", "mha_ffn_workspace_size",
-           "mha_ffn_forward", "mha_sublayer_workspace_size", "mha_sublayer_forward")
+           "mha_ffn_forward", "mha_sublayer_workspace_size", "mha_sublayer_forward",
+           "mha_decode_workspace_size", "mha_kv_cache_prefill", "mha_decode_step")
 
 
 class MHAError(RuntimeError):
@@ -84,6 +85,12 @@ def load(path: str | None = None):
         lib.mha_sublayer_forward.restype = i
         lib.mha_sublayer_forward.argtypes = ([i, vp, vp, vp, vp, ctypes.c_float, i] + [vp] * 8 + [i] * 5
                                              + [ctypes.POINTER(MaskT), vp, vp, sz, vp])
+        lib.mha_decode_workspace_size.restype = sz
+        lib.mha_decode_workspace_size.argtypes = [i] * 4
+        lib.mha_kv_cache_prefill.restype = i
+        lib.mha_kv_cache_prefill.argtypes = [i] + [vp] * 5 + [i] * 4 + [vp, vp, i, vp]
+        lib.mha_decode_step.restype = i
+        lib.mha_decode_step.argtypes = [i] + [vp] * 9 + [i] * 3 + [vp, vp, vp, i, vp, vp, sz, vp]
         lib.mha_forward_noalloc.restype = i
         lib.mha_forward_noalloc.argtypes = [i] + [vp] * 11 + [i] * 5 + [ctypes.POINTER(MaskT), vp, vp, vp]
         _lib = lib
@@ -195,6 +202,28 @@ def mha_forward_noalloc(query, key, value, w_q, b_q, w_k, b_k, w_v, b_v, w_o, b_
         _dtype_code(query), _ptr(query), _ptr(key), _ptr(value), _ptr(w_q), _ptr(b_q), _ptr(w_k),
         _ptr(b_k), _ptr(w_v), _ptr(b_v), _ptr(w_o), _ptr(b_o), B, Lq, Lk, d, h,
         ctypes.byref(mask) if mask is not None else None, _ptr(out), _ptr(p_attn), _stream(stream)))
+
+
+def decode_workspace_size(B: int, d_model: int, h: int, L_max: int) -> int:
+    return int(load().mha_decode_workspace_size(B, d_model, h, L_max))
+
+
+def mha_kv_cache_prefill(x, w_k, b_k, w_v, b_v, h, *, k_cache, v_cache, stream=None):
+    """Project x [B, T, d_model] into positions 0..T-1 of the caches [B, h, L_max, 64]."""
+    B, T, d = x.shape
+    _check(load().mha_kv_cache_prefill(
+        _dtype_code(x), _ptr(x), _ptr(w_k), _ptr(b_k), _ptr(w_v), _ptr(b_v), B, T, d, h, _ptr(k_cache),
+        _ptr(v_cache), k_cache.shape[2], _stream(stream)))
+
+
+def mha_decode_step(x_new, w_q, b_q, w_k, b_k, w_v, b_v, w_o, b_o, h, *, k_cache, v_cache, cache_len, out,
+                    workspace, stream=None):
+    """One decoding step: x_new [B, d_model] -> out [B, d_model]; appends to the caches, bumps cache_len."""
+    B, d = x_new.shape
+    _check(load().mha_decode_step(
+        _dtype_code(x_new), _ptr(x_new), _ptr(w_q), _ptr(b_q), _ptr(w_k), _ptr(b_k), _ptr(w_v), _ptr(b_v),
+        _ptr(w_o), _ptr(b_o), B, d, h, _ptr(k_cache), _ptr(v_cache), _ptr(cache_len), k_cache.shape[2],
+        _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 LN_UNBIASED_STD, LN_TORCH = 0, 1

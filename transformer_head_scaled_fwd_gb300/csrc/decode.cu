@@ -1,0 +1,196 @@
+// decode.cu -- incremental decoding: one new query per sequence against a
+// key/value cache.
+//
+// At prediction time the d2l Transformer decoder (d2l Transformer chapter
+// summary, DecoderBlock: state[2] keeps the representations decoded so far and
+// torch.cat appends the new one, used as keys and values) attends from the
+// newest token to every token decoded so far, itself included. Caching the
+// projected keys and values instead of the raw representations gives the same
+// result: attention() of "The Annotated Transformer" ("Attention") over all
+// cached keys, no mask needed (every cached position precedes the query).
+//
+// Kernels (HBM-bound: the cache is read once per step):
+//   kv_append_kernel    copies the new token's projected k, v (head-split) into
+//                       the caches at position cache_len[b] and increments it.
+//   decode_attn_kernel  split-K over the cached keys: each CTA takes a chunk of
+//                       keys of one (batch, head); a warp scores 32 keys at a
+//                       time (one key row per lane, 128-byte loads), keeps an
+//                       online softmax (running max and sum) and accumulates
+//                       p.V with two output features per lane; the CTA's warps
+//                       merge and write a partial (max, sum, o[64]).
+//   decode_combine_kernel  merges the partials of a (batch, head) and writes
+//                       its 64-wide slab of the concatenated context.
+#include <math_constants.h>
+
+#include "mha_internal.h"
+#include "ptx.cuh"
+
+namespace mha {
+namespace {
+
+constexpr int kD = 64;
+constexpr int kWarps = 4;
+
+__global__ void __launch_bounds__(256) kv_append_kernel(const DecodeParams p) {
+    const int b = blockIdx.x;
+    const int pos = p.cache_len[b];
+    __syncthreads();   // every thread has read the old length before it is incremented
+    if (pos < 0 || pos >= p.L_max) {
+        if (threadIdx.x == 0) atomicCAS(p.status, 0, 0x301);   // cache full: nothing appended
+        return;
+    }
+    // KVh of the step is [1, 2, h, B, 64]: k of (b, head) at ((head) * B + b) * 64, v after h planes
+    for (int e = threadIdx.x; e < p.h * kD / 8; e += blockDim.x) {
+        const int head = e / (kD / 8);
+        const int c8 = e % (kD / 8);
+        const long src = (static_cast<long>(head) * p.B + b) * kD + c8 * 8;
+        const long vsrc = (static_cast<long>(p.h + head) * p.B + b) * kD + c8 * 8;
+        const long dst = ((static_cast<long>(b) * p.h + head) * p.L_max + pos) * kD + c8 * 8;
+        *reinterpret_cast<uint4*>(p.k_cache + dst) = *reinterpret_cast<const uint4*>(p.kv_new + src);
+        *reinterpret_cast<uint4*>(p.v_cache + dst) = *reinterpret_cast<const uint4*>(p.kv_new + vsrc);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) p.cache_len[b] = pos + 1;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__global__ void __launch_bounds__(32 * kWarps) decode_attn_kernel(const DecodeParams p) {
+    __shared__ float sm_m[kWarps], sm_l[kWarps];
+    __shared__ float sm_o[kWarps][kD];
+    const int bh = blockIdx.y;
+    const int b = bh / p.h;
+    const int head = bh - b * p.h;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int n = min(max(p.cache_len[b], 0), p.L_max);
+    const int chunk = ((n + p.n_split - 1) / p.n_split + 31) & ~31;
+    const int c0 = blockIdx.x * chunk;
+    const int c1 = min(n, c0 + chunk);
+
+    // the query row of (b, head), fp32 in registers (same for every lane)
+    const __nv_bfloat16* qp = p.q_new + (static_cast<long>(head) * p.B + b) * kD;
+    float q[kD];
+#pragma unroll
+    for (int c = 0; c < kD; c += 8) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(qp + c);
+        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(h2[e]);
+            q[c + 2 * e] = f.x * p.scale_log2;   // scores in log2 units
+            q[c + 2 * e + 1] = f.y * p.scale_log2;
+        }
+    }
+    const __nv_bfloat16* K = p.k_cache + static_cast<long>(bh) * p.L_max * kD;
+    const __nv_bfloat16* V = p.v_cache + static_cast<long>(bh) * p.L_max * kD;
+    float m = -CUDART_INF_F, l = 0.0f, o0 = 0.0f, o1 = 0.0f;
+    for (int g = c0 + 32 * warp; g < c1; g += 32 * kWarps) {
+        const int key = g + lane;
+        float s = -CUDART_INF_F;
+        if (key < c1) {
+            const __nv_bfloat16* kr = K + static_cast<long>(key) * kD;
+            float acc = 0.0f;
+#pragma unroll
+            for (int c = 0; c < kD; c += 8) {
+                const uint4 raw = *reinterpret_cast<const uint4*>(kr + c);
+                const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __bfloat1622float2(h2[e]);
+                    acc = fmaf(q[c + 2 * e], f.x, acc);
+                    acc = fmaf(q[c + 2 * e + 1], f.y, acc);
+                }
+            }
+            s = acc;
+        }
+        const float m_new = fmaxf(m, warp_max(s));   // finite: key g < c1 always exists
+        const float alpha = ex2_approx(m - m_new);
+        const float pj = ex2_approx(s - m_new);
+        l = l * alpha + warp_sum(pj);
+        o0 *= alpha;
+        o1 *= alpha;
+        const int cnt = min(32, c1 - g);
+        for (int j = 0; j < cnt; ++j) {
+            const float w = __shfl_sync(0xffffffffu, pj, j);
+            const float2 v = __bfloat1622float2(
+                *reinterpret_cast<const __nv_bfloat162*>(V + static_cast<long>(g + j) * kD + 2 * lane));
+            o0 = fmaf(w, v.x, o0);
+            o1 = fmaf(w, v.y, o1);
+        }
+        m = m_new;
+    }
+    if (lane == 0) {
+        sm_m[warp] = m;
+        sm_l[warp] = l;
+    }
+    sm_o[warp][2 * lane] = o0;
+    sm_o[warp][2 * lane + 1] = o1;
+    __syncthreads();
+    if (warp == 0) {
+        float M = -CUDART_INF_F;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w]);
+        float L = 0.0f, a0 = 0.0f, a1 = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const float f = (sm_m[w] == -CUDART_INF_F) ? 0.0f : ex2_approx(sm_m[w] - M);
+            L += sm_l[w] * f;
+            a0 += sm_o[w][2 * lane] * f;
+            a1 += sm_o[w][2 * lane + 1] * f;
+        }
+        float* part = p.partial + (static_cast<long>(bh) * p.n_split + blockIdx.x) * (kD + 2);
+        if (lane == 0) {
+            part[0] = M;
+            part[1] = L;
+        }
+        part[2 + 2 * lane] = a0;
+        part[3 + 2 * lane] = a1;
+    }
+}
+
+__global__ void __launch_bounds__(kD) decode_combine_kernel(const DecodeParams p) {
+    const int bh = blockIdx.x;
+    const int b = bh / p.h;
+    const int head = bh - b * p.h;
+    const int c = threadIdx.x;
+    const float* part = p.partial + static_cast<long>(bh) * p.n_split * (kD + 2);
+    float M = -CUDART_INF_F;
+    for (int s = 0; s < p.n_split; ++s) M = fmaxf(M, part[s * (kD + 2)]);
+    float L = 0.0f, acc = 0.0f;
+    for (int s = 0; s < p.n_split; ++s) {
+        const float ms = part[s * (kD + 2)];
+        if (ms == -CUDART_INF_F) continue;   // empty chunk
+        const float f = ex2_approx(ms - M);
+        L += part[s * (kD + 2) + 1] * f;
+        acc += part[s * (kD + 2) + 2 + c] * f;
+    }
+    // ctx of the step is [1, B, d_model]: the head's slab of row b
+    p.ctx[static_cast<long>(b) * p.h * kD + head * kD + c] = __float2bfloat16_rn(acc / L);
+}
+
+}  // namespace
+
+cudaError_t launch_kv_append(const DecodeParams& p, cudaStream_t s) {
+    kv_append_kernel<<<p.B, 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode_attention(const DecodeParams& p, cudaStream_t s) {
+    decode_attn_kernel<<<dim3(p.n_split, p.B * p.h), 32 * kWarps, 0, s>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    decode_combine_kernel<<<p.B * p.h, kD, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace mha

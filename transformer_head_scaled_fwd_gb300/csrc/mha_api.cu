@@ -98,10 +98,12 @@ mha_status_t map_weight(CUtensorMap* m, const void* base, int N, int K) {
     const uint32_t box[2] = {64, (uint32_t)mha::kGemmBN};
     return encode_bf16(m, base, 2, dims, str, box, "weight");
 }
-// head-split [B, slabs, L, 64] as {64, L, slabs, B}, box {64, 128, 1, 1}
-mha_status_t map_heads4(CUtensorMap* m, const void* base, int B, int slabs, int L) {
+// head-split [B, slabs, L_stride, 64] with the first L rows of each plane used, as
+// {64, L, slabs, B}, box {64, 128, 1, 1}
+mha_status_t map_heads4(CUtensorMap* m, const void* base, int B, int slabs, int L, int L_stride = 0) {
+    if (L_stride <= 0) L_stride = L;
     const uint64_t dims[4] = {64, (uint64_t)L, (uint64_t)slabs, (uint64_t)B};
-    const uint64_t str[3] = {128, (uint64_t)L * 128, (uint64_t)slabs * L * 128};
+    const uint64_t str[3] = {128, (uint64_t)L_stride * 128, (uint64_t)slabs * L_stride * 128};
     const uint32_t box[4] = {64, 128, 1, 1};
     return encode_bf16(m, base, 4, dims, str, box, "head-split output");
 }
@@ -474,6 +476,109 @@ mha_status_t mha_sublayer_forward(mha_dtype_t dt, const void* x, const void* mem
     Layout Lo;
     layout_of(dt, B, L, Lk, d_model, h, &Lo);
     return output_projection_impl(dt, w_o, b_o, x, B, L, d_model, h, out, Lo, mws, s);
+}
+
+static int decode_split(int B, int h, int L_max) {
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int n = (4 * sms + B * h - 1) / (B * h);
+    n = std::min(n, (L_max + 63) / 64);
+    return std::max(1, std::min(n, mha::kDecodeMaxSplit));
+}
+
+size_t mha_decode_workspace_size(int B, int d_model, int h, int L_max) {
+    if (B <= 0 || d_model <= 0 || h <= 0 || L_max <= 0 || d_model % h != 0) return 0;
+    const size_t ws = mha_workspace_size(MHA_BF16, 1, B, B, d_model, h);
+    return ws + align256(sizeof(float) * (mha::kAttnD + 2) * B * h * static_cast<size_t>(mha::kDecodeMaxSplit));
+}
+
+mha_status_t mha_kv_cache_prefill(mha_dtype_t dt, const void* x, const void* w_k, const void* b_k, const void* w_v,
+                                  const void* b_v, int B, int T, int d_model, int h, void* k_cache, void* v_cache,
+                                  int L_max, void* stream) {
+    if (dt != MHA_BF16) return fail(MHA_ERR_UNSUPPORTED, "the key/value cache is implemented for bf16 only");
+    mha_status_t st = check_sizes(dt, B, T, T, d_model, h);
+    if (st != MHA_OK) return st;
+    if (T > L_max) return fail(MHA_ERR_INVALID_ARG, "T (%d) exceeds the cache length L_max (%d)", T, L_max);
+    if (!x || !w_k || !w_v || !k_cache || !v_cache)
+        return fail(MHA_ERR_INVALID_ARG, "x, W_k, W_v and the caches must not be NULL");
+    const void* ptrs[7] = {x, w_k, b_k, w_v, b_v, k_cache, v_cache};
+    for (const void* ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return fail(MHA_ERR_INVALID_ARG, "bf16 tensors must be 16-byte aligned");
+    if ((st = get_encoder()) != MHA_OK) return st;
+    mha::GemmParams p;
+    memset(&p, 0, sizeof(p));
+    const void* W[2] = {w_k, w_v};
+    const void* bias[2] = {b_k, b_v};
+    void* cache[2] = {k_cache, v_cache};
+    for (int g = 0; g < 2; ++g) {
+        if ((st = map_rows(&p.a[g], x, B, T, d_model, "prefill input")) != MHA_OK) return st;
+        if ((st = map_weight(&p.w[g], W[g], d_model, d_model)) != MHA_OK) return st;
+        if ((st = map_heads4(&p.out[g], cache[g], B, h, T, L_max)) != MHA_OK) return st;
+        p.g[g].L = T;
+        p.g[g].tiles_per_b = (T + mha::kGemmBM - 1) / mha::kGemmBM;
+        p.g[g].m_tiles = B * p.g[g].tiles_per_b;
+        p.g[g].out_j0 = 0;
+        p.g[g].bias = static_cast<const __nv_bfloat16*>(bias[g]);
+    }
+    p.ngroups = 2;
+    p.K = d_model;
+    p.N = d_model;
+    p.status = device_status_ptr();
+    if (!p.status) return fail(MHA_ERR_CUDA, "device status word unavailable");
+    cudaError_t e = mha::launch_gemm_tc(p, p.g[0].m_tiles, as_stream(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cache prefill launch");
+    return MHA_OK;
+}
+
+mha_status_t mha_decode_step(mha_dtype_t dt, const void* x_new, const void* w_q, const void* b_q, const void* w_k,
+                             const void* b_k, const void* w_v, const void* b_v, const void* w_o, const void* b_o,
+                             int B, int d_model, int h, void* k_cache, void* v_cache, int32_t* cache_len,
+                             int L_max, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+    if (dt != MHA_BF16) return fail(MHA_ERR_UNSUPPORTED, "incremental decoding is implemented for bf16 only");
+    mha_status_t st = check_sizes(dt, 1, B, B, d_model, h);
+    if (st != MHA_OK) return st;
+    if (L_max <= 0) return fail(MHA_ERR_INVALID_ARG, "L_max must be positive");
+    if (!x_new || !w_q || !w_k || !w_v || !w_o || !k_cache || !v_cache || !cache_len || !out)
+        return fail(MHA_ERR_INVALID_ARG, "x_new, weights, caches, cache_len and out must not be NULL");
+    const size_t need = mha_decode_workspace_size(B, d_model, h, L_max);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(MHA_ERR_INVALID_ARG, "workspace must be non-NULL and 256-byte aligned");
+    if (workspace_bytes < need) return fail(MHA_ERR_INVALID_ARG, "workspace too small: %zu < %zu", workspace_bytes, need);
+    const void* ptrs[11] = {x_new, w_q, b_q, w_k, b_k, w_v, b_v, w_o, b_o, k_cache, v_cache};
+    for (const void* ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return fail(MHA_ERR_INVALID_ARG, "bf16 tensors must be 16-byte aligned");
+    if (!aligned16(out)) return fail(MHA_ERR_INVALID_ARG, "bf16 tensors must be 16-byte aligned");
+    const size_t ws_mha = mha_workspace_size(MHA_BF16, 1, B, B, d_model, h);
+    // 1. q, k, v of the B new tokens: the projection GEMM on a [1, B, d_model] view
+    if ((st = mha_qkv_projection(dt, x_new, x_new, x_new, w_q, b_q, w_k, b_k, w_v, b_v, 1, B, B, d_model, h,
+                                 workspace, ws_mha, stream)) != MHA_OK)
+        return st;
+    Layout L;
+    layout_of(dt, 1, B, B, d_model, h, &L);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    mha::DecodeParams p{};
+    p.q_new = reinterpret_cast<const __nv_bfloat16*>(ws + L.q);
+    p.kv_new = reinterpret_cast<const __nv_bfloat16*>(ws + L.kv);
+    p.k_cache = static_cast<__nv_bfloat16*>(k_cache);
+    p.v_cache = static_cast<__nv_bfloat16*>(v_cache);
+    p.cache_len = cache_len;
+    p.ctx = reinterpret_cast<__nv_bfloat16*>(ws + L.ctx);
+    p.partial = reinterpret_cast<float*>(ws + ws_mha);
+    p.B = B;
+    p.h = h;
+    p.L_max = L_max;
+    p.n_split = decode_split(B, h, L_max);
+    p.scale_log2 = static_cast<float>(1.4426950408889634 / 8.0);
+    p.status = device_status_ptr();
+    if (!p.status) return fail(MHA_ERR_CUDA, "device status word unavailable");
+    const cudaStream_t s = as_stream(stream);
+    // 2. append k, v at cache_len[b] (incremented); 3. attention over the cache; 4. merge
+    cudaError_t e = mha::launch_kv_append(p, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cache append launch");
+    e = mha::launch_decode_attention(p, s);
+    if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
+    // 5. out = ctx W_o^T + b_o
+    return output_projection_impl(dt, w_o, b_o, nullptr, 1, B, d_model, h, out, L, ws, s);
 }
 
 size_t mha_ffn_workspace_size(mha_dtype_t dt, int B, int L, int d_model, int d_ff) {

@@ -123,6 +123,23 @@ struct F32AttnParams {
 };
 cudaError_t launch_attn_f32(const F32AttnParams& p, cudaStream_t s);
 
+// ------------------------------------------------------------ incremental decoding (d_k = 64, bf16)
+struct DecodeParams {
+    const __nv_bfloat16* q_new;    // Qh of the step [1, h, B, 64]
+    const __nv_bfloat16* kv_new;   // KVh of the step [1, 2, h, B, 64]
+    __nv_bfloat16* k_cache;        // [B, h, L_max, 64]
+    __nv_bfloat16* v_cache;        // [B, h, L_max, 64]
+    int32_t* cache_len;            // [B], incremented by the append kernel
+    __nv_bfloat16* ctx;            // [1, B, h * 64]
+    float* partial;                // [B * h, n_split, 66]: max (log2 units), sum, o[64]
+    int B, h, L_max, n_split;
+    float scale_log2;
+    int* status;
+};
+constexpr int kDecodeMaxSplit = 64;
+cudaError_t launch_kv_append(const DecodeParams& p, cudaStream_t s);
+cudaError_t launch_decode_attention(const DecodeParams& p, cudaStream_t s);
+
 // ------------------------------------------------------------ LayerNorm (rows of length d)
 struct LayerNormParams {
     const void* x;       // [rows, d]
