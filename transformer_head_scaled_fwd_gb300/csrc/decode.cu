@@ -96,34 +96,41 @@ __global__ void __launch_bounds__(32 * kWarps) decode_attn_kernel(const DecodePa
     float m = -CUDART_INF_F, l = 0.0f, o0 = 0.0f, o1 = 0.0f;
     for (int g = c0 + 32 * warp; g < c1; g += 32 * kWarps) {
         const int key = g + lane;
-        float s = -CUDART_INF_F;
-        if (key < c1) {
-            const __nv_bfloat16* kr = K + static_cast<long>(key) * kD;
-            float acc = 0.0f;
+        const int cnt = c1 - g;
+        // issue this group's key row (one per lane) and value rows (one 128-byte row per key,
+        // two features per lane) together, so both memory latencies overlap
+        uint4 kraw[kD / 8];
 #pragma unroll
-            for (int c = 0; c < kD; c += 8) {
-                const uint4 raw = *reinterpret_cast<const uint4*>(kr + c);
-                const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+        for (int c = 0; c < kD / 8; ++c)
+            kraw[c] = (key < c1) ? *reinterpret_cast<const uint4*>(K + static_cast<long>(key) * kD + 8 * c)
+                                 : make_uint4(0, 0, 0, 0);
+        __nv_bfloat162 vr[32];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 f = __bfloat1622float2(h2[e]);
-                    acc = fmaf(q[c + 2 * e], f.x, acc);
-                    acc = fmaf(q[c + 2 * e + 1], f.y, acc);
-                }
+        for (int j = 0; j < 32; ++j)
+            vr[j] = (j < cnt) ? *reinterpret_cast<const __nv_bfloat162*>(V + static_cast<long>(g + j) * kD + 2 * lane)
+                              : __floats2bfloat162_rn(0.0f, 0.0f);
+        float acc = 0.0f;
+#pragma unroll
+        for (int c = 0; c < kD / 8; ++c) {
+            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&kraw[c]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __bfloat1622float2(h2[e]);
+                acc = fmaf(q[8 * c + 2 * e], f.x, acc);
+                acc = fmaf(q[8 * c + 2 * e + 1], f.y, acc);
             }
-            s = acc;
         }
+        const float s = (key < c1) ? acc : -CUDART_INF_F;
         const float m_new = fmaxf(m, warp_max(s));   // finite: key g < c1 always exists
         const float alpha = ex2_approx(m - m_new);
-        const float pj = ex2_approx(s - m_new);
+        const float pj = ex2_approx(s - m_new);      // 0 for keys past the chunk
         l = l * alpha + warp_sum(pj);
         o0 *= alpha;
         o1 *= alpha;
-        const int cnt = min(32, c1 - g);
-        for (int j = 0; j < cnt; ++j) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
             const float w = __shfl_sync(0xffffffffu, pj, j);
-            const float2 v = __bfloat1622float2(
-                *reinterpret_cast<const __nv_bfloat162*>(V + static_cast<long>(g + j) * kD + 2 * lane));
+            const float2 v = __bfloat1622float2(vr[j]);
             o0 = fmaf(w, v.x, o0);
             o1 = fmaf(w, v.y, o1);
         }

@@ -481,8 +481,8 @@ mha_status_t mha_sublayer_forward(mha_dtype_t dt, const void* x, const void* mem
 static int decode_split(int B, int h, int L_max) {
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    int n = (4 * sms + B * h - 1) / (B * h);
-    n = std::min(n, (L_max + 63) / 64);
+    int n = (8 * sms + B * h - 1) / (B * h);    // about 8 CTAs of 4 warps per SM
+    n = std::min(n, (L_max + 127) / 128);      // at least 128 keys per chunk
     return std::max(1, std::min(n, mha::kDecodeMaxSplit));
 }
 
