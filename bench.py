@@ -35,6 +35,7 @@ DESCRIPTION = {
     "dec": "decoder masked self-attention B32 L256 d_model512 h8 d_k64, causal AND key padding U{128..256}",
     "xattn": "encoder-decoder attention B16 Lq256 Lk320 d_model1024 h16 d_k64, memory as key/value, padding U{160..320}",
     "long": "long-sequence causal self-attention B4 L8192 d_model1024 h16 d_k64",
+    "long_d128": "long-sequence causal self-attention B4 L8192 d_model1024 h8 d_k128",
 }
 KERNEL_SOURCES = {"qkv_projection_gemm": "gemm_tc.cu", "attention_core": "attn_tc.cu",
                   "output_projection_gemm": "gemm_tc.cu"}
@@ -575,7 +576,7 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--workload", default=WORKLOAD, choices=["enc", "dec", "xattn", "long"])
+    ap.add_argument("--workload", default=WORKLOAD, choices=["enc", "dec", "xattn", "long", "long_d128"])
     ap.add_argument("--ref-prefix", type=int, default=2048, help="causal prefix length of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-batch", type=int, default=16)

@@ -36,7 +36,7 @@
  *   - dt selects the storage type of query/key/value/weights/biases/out and of
  *     the workspace tensors: MHA_F32 (fp32 everywhere, fp32 SIMT arithmetic,
  *     any d_k <= 256) or MHA_BF16 (bf16 storage, fp32 accumulation on the
- *     tensor cores, d_k == 64 only). p_attn is always fp32.
+ *     tensor cores, d_k = 64 or 128). p_attn is always fp32.
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and the call returns without waiting for it.
  *   - Arguments are validated on the host before anything is enqueued. On a
@@ -60,7 +60,7 @@ extern "C" {
 typedef enum {
     MHA_OK = 0,
     MHA_ERR_INVALID_ARG = 1,   /* bad size, null required pointer, small workspace */
-    MHA_ERR_UNSUPPORTED = 2,   /* valid per the pages but not implemented (e.g. bf16 with d_k != 64) */
+    MHA_ERR_UNSUPPORTED = 2,   /* valid per the pages but not implemented (e.g. bf16 with d_k = 96) */
     MHA_ERR_CUDA = 3           /* a CUDA call failed; see mha_last_error() */
 } mha_status_t;
 
@@ -229,7 +229,7 @@ mha_status_t mha_sublayer_forward(mha_dtype_t dt, const void* x, const void* mem
                                   void* stream);
 
 /*
- * Incremental decoding with a key/value cache (bf16, d_k = 64).
+ * Incremental decoding with a key/value cache (bf16, d_k = 64 only).
  * At prediction time the d2l Transformer decoder (d2l Transformer chapter, DecoderBlock:
  * state[2] keeps the representations decoded so far and torch.cat appends the new one as
  * keys and values) attends from the newest token to every token so far, itself included.

@@ -62,7 +62,7 @@ def test_validation_without_gpu(lib):
     assert _call_forward(lib, d=130, h=4) == binding.MHA_ERR_INVALID_ARG          # d % h != 0
     assert b"d_model % h" in lib.mha_last_error()
     assert _call_forward(lib, B_=0) == binding.MHA_ERR_INVALID_ARG
-    assert _call_forward(lib, d=256, h=2) == binding.MHA_ERR_UNSUPPORTED          # bf16 d_k = 128
+    assert _call_forward(lib, d=192, h=2) == binding.MHA_ERR_UNSUPPORTED          # bf16 d_k = 96
     assert _call_forward(lib, dt=binding.MHA_F32, d=1024, h=2) == binding.MHA_ERR_UNSUPPORTED
     assert _call_forward(lib, dt=7) == binding.MHA_ERR_INVALID_ARG
     m = binding.MaskT(); m.causal = 1

@@ -407,18 +407,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
 constexpr int kPRows = 32;     // query rows per block
 constexpr int kPKeys = 128;    // keys per pass (one per thread)
 
+template <int D>
 __global__ void __launch_bounds__(kPKeys) pattn_bf16_kernel(const PattnParams p) {
-    __shared__ float qs[kPRows][kAttnD];
+    __shared__ float qs[kPRows][D];
     __shared__ float2 st[kPRows];
     const int bh = blockIdx.y;
     const int b = bh / p.h;
     const int head = bh - b * p.h;
     const int i0 = blockIdx.x * kPRows;
-    const __nv_bfloat16* q = p.q + (static_cast<long>(bh) * p.Lq) * kAttnD;
-    const __nv_bfloat16* k = p.kv + (static_cast<long>(b) * 2 * p.h + head) * p.Lk * kAttnD;
-    for (int e = threadIdx.x; e < kPRows * kAttnD; e += blockDim.x) {
-        const int r = e / kAttnD, c = e % kAttnD;
-        qs[r][c] = (i0 + r < p.Lq) ? __bfloat162float(q[static_cast<long>(i0 + r) * kAttnD + c]) : 0.0f;
+    const __nv_bfloat16* q = p.q + (static_cast<long>(bh) * p.Lq) * D;
+    const __nv_bfloat16* k = p.kv + (static_cast<long>(b) * 2 * p.h + head) * p.Lk * D;
+    for (int e = threadIdx.x; e < kPRows * D; e += blockDim.x) {
+        const int r = e / D, c = e % D;
+        qs[r][c] = (i0 + r < p.Lq) ? __bfloat162float(q[static_cast<long>(i0 + r) * D + c]) : 0.0f;
     }
     for (int r = threadIdx.x; r < kPRows; r += blockDim.x)
         st[r] = (i0 + r < p.Lq) ? reinterpret_cast<const float2*>(p.stats)[static_cast<long>(bh) * p.Lq + i0 + r]
@@ -429,10 +430,10 @@ __global__ void __launch_bounds__(kPKeys) pattn_bf16_kernel(const PattnParams p)
     for (int k0 = 0; k0 < p.Lk; k0 += kPKeys) {
         const int kj = k0 + threadIdx.x;
         if (kj >= p.Lk) continue;
-        float kr[kAttnD];
+        float kr[D];
 #pragma unroll
-        for (int c = 0; c < kAttnD; c += 8) {
-            const uint4 raw = *reinterpret_cast<const uint4*>(k + static_cast<long>(kj) * kAttnD + c);
+        for (int c = 0; c < D; c += 8) {
+            const uint4 raw = *reinterpret_cast<const uint4*>(k + static_cast<long>(kj) * D + c);
             const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -446,7 +447,7 @@ __global__ void __launch_bounds__(kPKeys) pattn_bf16_kernel(const PattnParams p)
             if (qi >= p.Lq) break;
             float dot = 0.f;
 #pragma unroll
-            for (int c = 0; c < kAttnD; ++c) dot = fmaf(qs[r][c], kr[c], dot);
+            for (int c = 0; c < D; ++c) dot = fmaf(qs[r][c], kr[c], dot);
             bool ok = !(p.causal && kj > qi) && kj < vl;
             if (ok && p.dense != nullptr) {
                 const long mrow = (p.dense_mq == 1) ? 0 : qi;
@@ -474,7 +475,10 @@ cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t s) {
 
 cudaError_t launch_pattn_bf16(const PattnParams& p, cudaStream_t s) {
     dim3 grid((p.Lq + kPRows - 1) / kPRows, p.B * p.h);
-    pattn_bf16_kernel<<<grid, kPKeys, 0, s>>>(p);
+    if (p.dk == 128)
+        pattn_bf16_kernel<128><<<grid, kPKeys, 0, s>>>(p);
+    else
+        pattn_bf16_kernel<64><<<grid, kPKeys, 0, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -224,8 +224,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
                     const uint8_t* src = base + kOffStage + sb * kSlabBytes;
                     if (p.out_plain)
                         tma_store_3d(&p.out[c.grp], src, n, c.l0, c.b);
-                    else
-                        tma_store_4d(&p.out[c.grp], src, 0, c.l0, G.out_j0 + n / 64, c.b);
+                    else   // slab n/64 of the group: head (n/64) / dk_slabs, half (n/64) % dk_slabs
+                        tma_store_5d(&p.out[c.grp], src, 0, (n / 64) % p.dk_slabs, c.l0,
+                                     G.out_j0 + (n / 64) / p.dk_slabs, c.b);
                     tma_store_commit();
                 }
                 ++slabs_issued;

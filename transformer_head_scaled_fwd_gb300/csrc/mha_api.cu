@@ -98,14 +98,23 @@ mha_status_t map_weight(CUtensorMap* m, const void* base, int N, int K) {
     const uint32_t box[2] = {64, (uint32_t)mha::kGemmBN};
     return encode_bf16(m, base, 2, dims, str, box, "weight");
 }
-// head-split [B, slabs, L_stride, 64] with the first L rows of each plane used, as
-// {64, L, slabs, B}, box {64, 128, 1, 1}
-mha_status_t map_heads4(CUtensorMap* m, const void* base, int B, int slabs, int L, int L_stride = 0) {
+// head-split [B, planes, L_stride, d_k] (first L rows of each plane used), d_k = 64 * dks, as
+// {64, dks, L, planes, B}: a 64-column slab is (0, half, row, plane, b); box {64, 1, 128, 1, 1}
+mha_status_t map_heads5(CUtensorMap* m, const void* base, int B, int planes, int L, int dks, int L_stride = 0) {
     if (L_stride <= 0) L_stride = L;
-    const uint64_t dims[4] = {64, (uint64_t)L, (uint64_t)slabs, (uint64_t)B};
-    const uint64_t str[3] = {128, (uint64_t)L_stride * 128, (uint64_t)slabs * L_stride * 128};
-    const uint32_t box[4] = {64, 128, 1, 1};
-    return encode_bf16(m, base, 4, dims, str, box, "head-split output");
+    const uint64_t row = 128ull * dks;
+    const uint64_t dims[5] = {64, (uint64_t)dks, (uint64_t)L, (uint64_t)planes, (uint64_t)B};
+    const uint64_t str[4] = {128, row, (uint64_t)L_stride * row, (uint64_t)planes * L_stride * row};
+    const uint32_t box[5] = {64, 1, 128, 1, 1};
+    return encode_bf16(m, base, 5, dims, str, box, "head-split output");
+}
+// head-split [planes, L, d_k] as {64, dks, L, planes}, box {64, 1, 128, 1} (attention loads)
+mha_status_t map_heads4d(CUtensorMap* m, const void* base, int planes, int L, int dks) {
+    const uint64_t row = 128ull * dks;
+    const uint64_t dims[4] = {64, (uint64_t)dks, (uint64_t)L, (uint64_t)planes};
+    const uint64_t str[3] = {128, row, (uint64_t)L * row};
+    const uint32_t box[4] = {64, 1, 128, 1};
+    return encode_bf16(m, base, 4, dims, str, box, "head-split input");
 }
 // head-split [planes, L, 64] as {64, L, planes}, box {64, 128, 1}
 mha_status_t map_heads3(CUtensorMap* m, const void* base, int planes, int L) {
@@ -131,8 +140,8 @@ mha_status_t check_sizes(mha_dtype_t dt, int B, int Lq, int Lk, int d, int h) {
                     h);
     if (d % h != 0) return fail(MHA_ERR_INVALID_ARG, "d_model %% h != 0 (d_model=%d, h=%d)", d, h);
     const int dk = d / h;
-    if (dt == MHA_BF16 && dk != 64)
-        return fail(MHA_ERR_UNSUPPORTED, "bf16 path implements d_k = 64 only (d_k = %d)", dk);
+    if (dt == MHA_BF16 && dk != 64 && dk != 128)
+        return fail(MHA_ERR_UNSUPPORTED, "bf16 path implements d_k = 64 and 128 (d_k = %d)", dk);
     if (dt == MHA_F32 && dk > 256) return fail(MHA_ERR_UNSUPPORTED, "fp32 path implements d_k <= 256 (d_k = %d)", dk);
     const double big = static_cast<double>(B) * h * Lq * Lk;
     if (static_cast<double>(B) * Lq * d > 4.0e9 || static_cast<double>(B) * Lk * d * 2 > 4.0e9 || big > 1.0e15)
@@ -248,9 +257,9 @@ mha_status_t mha_qkv_projection(mha_dtype_t dt, const void* query, const void* k
         if ((st = map_rows(&p.a[g], A[g], B, Ls[g], d_model, "projection input")) != MHA_OK) return st;
         if ((st = map_weight(&p.w[g], W[g], d_model, d_model)) != MHA_OK) return st;
         if (g == 0) {
-            if ((st = map_heads4(&p.out[g], ws + L.q, B, h, L_q)) != MHA_OK) return st;
+            if ((st = map_heads5(&p.out[g], ws + L.q, B, h, L_q, dk / 64)) != MHA_OK) return st;
         } else {
-            if ((st = map_heads4(&p.out[g], ws + L.kv, B, 2 * h, L_k)) != MHA_OK) return st;
+            if ((st = map_heads5(&p.out[g], ws + L.kv, B, 2 * h, L_k, dk / 64)) != MHA_OK) return st;
         }
         p.g[g].L = Ls[g];
         p.g[g].tiles_per_b = (Ls[g] + mha::kGemmBM - 1) / mha::kGemmBM;
@@ -263,6 +272,7 @@ mha_status_t mha_qkv_projection(mha_dtype_t dt, const void* query, const void* k
     p.K = d_model;
     p.N = d_model;
     p.out_plain = 0;
+    p.dk_slabs = dk / 64;
     p.status = device_status_ptr();
     if (!p.status) return fail(MHA_ERR_CUDA, "device status word unavailable");
     cudaError_t e = mha::launch_gemm_tc(p, max_m, s);
@@ -302,17 +312,23 @@ mha_status_t mha_attention_core(mha_dtype_t dt, int B, int L_q, int L_k, int d_m
     if ((st = get_encoder()) != MHA_OK) return st;
     mha::AttnParams p;
     memset(&p, 0, sizeof(p));
-    if ((st = map_heads3(&p.q_map, ws + L.q, B * h, L_q)) != MHA_OK) return st;
-    if ((st = map_heads3(&p.kv_map, ws + L.kv, B * 2 * h, L_k)) != MHA_OK) return st;
+    if (dk == 64) {
+        if ((st = map_heads3(&p.q_map, ws + L.q, B * h, L_q)) != MHA_OK) return st;
+        if ((st = map_heads3(&p.kv_map, ws + L.kv, B * 2 * h, L_k)) != MHA_OK) return st;
+    } else {
+        if ((st = map_heads4d(&p.q_map, ws + L.q, B * h, L_q, dk / 64)) != MHA_OK) return st;
+        if ((st = map_heads4d(&p.kv_map, ws + L.kv, B * 2 * h, L_k, dk / 64)) != MHA_OK) return st;
+    }
     if ((st = map_rows(&p.ctx_map, ws + L.ctx, B, L_q, d_model, "context")) != MHA_OK) return st;
     p.B = B; p.h = h; p.Lq = L_q; p.Lk = L_k;
     p.causal = causal; p.valid_lens = vl; p.dense = dense; p.dense_mq = dmq;
     p.stats = p_attn ? reinterpret_cast<float*>(ws + L.stat) : nullptr;
     p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(dk)));
-    p.q_pairs = (L_q + 2 * mha::kAttnBM - 1) / (2 * mha::kAttnBM);
+    const int q_rows = dk == 64 ? 2 * mha::kAttnBM : mha::kAttnBM;   // query rows per CTA
+    p.q_pairs = (L_q + q_rows - 1) / q_rows;
     p.status = device_status_ptr();
     if (!p.status) return fail(MHA_ERR_CUDA, "device status word unavailable");
-    cudaError_t e = mha::launch_attn_tc(p, s);
+    cudaError_t e = dk == 64 ? mha::launch_attn_tc(p, s) : mha::launch_attn_tc_d128(p, s);
     if (e != cudaSuccess) return cuda_fail(e, "attention launch");
     if (p_attn) {
         mha::PattnParams pp{};
@@ -323,6 +339,7 @@ mha_status_t mha_attention_core(mha_dtype_t dt, int B, int L_q, int L_k, int d_m
         pp.B = B; pp.h = h; pp.Lq = L_q; pp.Lk = L_k;
         pp.causal = causal; pp.valid_lens = vl; pp.dense = dense; pp.dense_mq = dmq;
         pp.scale_log2 = p.scale_log2;
+        pp.dk = dk;
         e = mha::launch_pattn_bf16(pp, s);
         if (e != cudaSuccess) return cuda_fail(e, "p_attn launch");
     }
@@ -498,6 +515,7 @@ mha_status_t mha_kv_cache_prefill(mha_dtype_t dt, const void* x, const void* w_k
     if (dt != MHA_BF16) return fail(MHA_ERR_UNSUPPORTED, "the key/value cache is implemented for bf16 only");
     mha_status_t st = check_sizes(dt, B, T, T, d_model, h);
     if (st != MHA_OK) return st;
+    if (d_model / h != 64) return fail(MHA_ERR_UNSUPPORTED, "the key/value cache is implemented for d_k = 64");
     if (T > L_max) return fail(MHA_ERR_INVALID_ARG, "T (%d) exceeds the cache length L_max (%d)", T, L_max);
     if (!x || !w_k || !w_v || !k_cache || !v_cache)
         return fail(MHA_ERR_INVALID_ARG, "x, W_k, W_v and the caches must not be NULL");
@@ -513,7 +531,7 @@ mha_status_t mha_kv_cache_prefill(mha_dtype_t dt, const void* x, const void* w_k
     for (int g = 0; g < 2; ++g) {
         if ((st = map_rows(&p.a[g], x, B, T, d_model, "prefill input")) != MHA_OK) return st;
         if ((st = map_weight(&p.w[g], W[g], d_model, d_model)) != MHA_OK) return st;
-        if ((st = map_heads4(&p.out[g], cache[g], B, h, T, L_max)) != MHA_OK) return st;
+        if ((st = map_heads5(&p.out[g], cache[g], B, h, T, 1, L_max)) != MHA_OK) return st;
         p.g[g].L = T;
         p.g[g].tiles_per_b = (T + mha::kGemmBM - 1) / mha::kGemmBM;
         p.g[g].m_tiles = B * p.g[g].tiles_per_b;
@@ -523,6 +541,7 @@ mha_status_t mha_kv_cache_prefill(mha_dtype_t dt, const void* x, const void* w_k
     p.ngroups = 2;
     p.K = d_model;
     p.N = d_model;
+    p.dk_slabs = 1;
     p.status = device_status_ptr();
     if (!p.status) return fail(MHA_ERR_CUDA, "device status word unavailable");
     cudaError_t e = mha::launch_gemm_tc(p, p.g[0].m_tiles, as_stream(stream));
@@ -537,6 +556,7 @@ mha_status_t mha_decode_step(mha_dtype_t dt, const void* x_new, const void* w_q,
     if (dt != MHA_BF16) return fail(MHA_ERR_UNSUPPORTED, "incremental decoding is implemented for bf16 only");
     mha_status_t st = check_sizes(dt, 1, B, B, d_model, h);
     if (st != MHA_OK) return st;
+    if (d_model / h != 64) return fail(MHA_ERR_UNSUPPORTED, "incremental decoding is implemented for d_k = 64");
     if (L_max <= 0) return fail(MHA_ERR_INVALID_ARG, "L_max must be positive");
     if (!x_new || !w_q || !w_k || !w_v || !w_o || !k_cache || !v_cache || !cache_len || !out)
         return fail(MHA_ERR_INVALID_ARG, "x_new, weights, caches, cache_len and out must not be NULL");

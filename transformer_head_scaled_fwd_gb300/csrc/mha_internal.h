@@ -28,7 +28,7 @@ struct GemmGroup {
     int L;             // rows per batch item
     int tiles_per_b;   // ceil(L / 128)
     int m_tiles;       // B * tiles_per_b
-    int out_j0;        // first 64-column slab of this group in a head-split output
+    int out_j0;        // first head plane of this group in a head-split output
     const __nv_bfloat16* bias;       // [N] or nullptr
     const __nv_bfloat16* residual;   // plain output only: [B, L, N] added after the bias, or nullptr
 };
@@ -36,12 +36,13 @@ struct GemmGroup {
 struct GemmParams {
     CUtensorMap a[3];     // {K, L, B}, box {64, 128, 1}
     CUtensorMap w[3];     // {K, N},    box {64, 256}
-    CUtensorMap out[3];   // head-split {64, L, slabs, B} box {64,128,1,1}, or plain {N, L, B} box {64,128,1}
+    CUtensorMap out[3];   // head-split {64, d_k/64, L, planes, B} box {64,1,128,1,1}, or plain {N, L, B} box {64,128,1}
     GemmGroup g[3];
     int ngroups;
     int K;
     int N;
     int out_plain;        // 1: plain [B, L, N] output
+    int dk_slabs;         // head-split output: d_k / 64 (64-column slabs per head)
     int relu;             // 1: max(0, .) after the bias (first FFN layer)
     int* status;
 };
@@ -73,11 +74,14 @@ struct AttnParams {
 
 size_t attn_tc_smem_bytes();
 cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t s);
+// d_k = 128: same parameters with q_map / kv_map as {64, 2, L, planes} and q_pairs = ceil(L_q / 128)
+cudaError_t launch_attn_tc_d128(const AttnParams& p, cudaStream_t s);
 
 // p_attn for the bf16 path from Qh, KVh and the row statistics.
 struct PattnParams {
-    const __nv_bfloat16* q;     // Qh [B, h, Lq, 64]
-    const __nv_bfloat16* kv;    // KVh [B, 2, h, Lk, 64]
+    const __nv_bfloat16* q;     // Qh [B, h, Lq, dk]
+    const __nv_bfloat16* kv;    // KVh [B, 2, h, Lk, dk]
+    int dk;                     // 64 or 128
     const float* stats;         // [B, h, Lq, 2]
     float* p_attn;              // [B, h, Lq, Lk]
     int B, h, Lq, Lk;

@@ -65,6 +65,9 @@ WORKLOADS = {
                       note="encoder-decoder attention, memory as key and value, padding U{160..320}"),
     "long": Workload("long", 4, "bf16", 4, 8192, 8192, 1024, 16, True, True,
                      note="long-sequence causal self-attention, causal mask only"),
+    # wider heads (d_k = 128): the same model width with h = 8
+    "long_d128": Workload("long_d128", 5, "bf16", 4, 8192, 8192, 1024, 8, True, True,
+                          note="long-sequence causal self-attention with d_k = 128"),
 }
 
 
