@@ -144,10 +144,13 @@ mha_status_t mha_output_projection(mha_dtype_t dt, const void* w_o, const void* 
  * buffer; weights, biases, mask parts and the workspace are device pointers as
  * above. The host buffers should be page-locked for the copies to be
  * asynchronous. `staging` is device memory of at least
- * mha_host_staging_size(...) bytes that receives the activations. Enqueues:
- * host->device copies of query (and key, value unless they alias query / each
- * other), the three stages, and the device->host copy of out; then returns
- * (the caller synchronises the stream before reading out).
+ * mha_host_staging_size(...) bytes that receives the activations. The call is
+ * pipelined over up to 4 chunks of sequences: a library-owned copy stream (one
+ * per device, created on first use) uploads chunk c+1 and downloads chunk c-1
+ * while `stream` computes chunk c (host->device copies of query, and of key
+ * and value unless they alias query / each other; the three stages; the
+ * device->host copy of out), ordered by events. When the call returns, all of
+ * it is enqueued behind `stream`: synchronise `stream` before reading out.
  */
 size_t mha_host_staging_size(mha_dtype_t dt, int B, int L_q, int L_k, int d_model,
                              int kv_distinct, int q_distinct);

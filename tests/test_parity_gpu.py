@@ -230,3 +230,30 @@ def test_invalid_arguments_leave_output_untouched():
     assert e.value.status == binding.MHA_ERR_UNSUPPORTED
     torch.cuda.synchronize()
     assert torch.all(out == 3.0)
+
+
+def test_forward_host_uneven_chunks_distinct_kv_and_masks():
+    """Host entry point pipelined over chunks of sequences: 5 sequences -> chunks of 2, 2, 1;
+    key != value != query, per-sequence valid lengths and a per-query dense mask (offset per chunk)."""
+    from transformer_head_scaled_fwd_gb300 import binding
+    from gpu_helpers import to_dev
+    B, Lq, Lk, d, h = 5, 70, 90, 256, 4
+    inp = W.random_case(110, B, Lq, Lk, d, h, kv_alias=False)
+    vl = [90, 3, 0, 45, 90]
+    dense = (np.random.default_rng(111).random((B, Lq, Lk)) < 0.8).astype(np.uint8)
+    dt = torch.bfloat16
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dt).pin_memory()
+    hq, hk, hv = pin(inp.query), pin(inp.key), pin(inp.value)
+    hout = torch.empty(B, Lq, d, dtype=dt).pin_memory()
+    Wd = {n: to_dev(a, dt) for n, a in inp.weights.items()}
+    staging = torch.empty(binding.host_staging_size(binding.MHA_BF16, B, Lq, Lk, d, True, True),
+                          dtype=torch.uint8, device="cuda")
+    ws = torch.empty(binding.workspace_size(binding.MHA_BF16, B, Lq, Lk, d, h), dtype=torch.uint8, device="cuda")
+    vld = torch.tensor(vl, dtype=torch.int32, device="cuda")
+    dmd = torch.from_numpy(dense).cuda()
+    binding.mha_forward_host(hq, hk, hv, Wd["w_q"], Wd["b_q"], Wd["w_k"], Wd["b_k"], Wd["w_v"], Wd["b_v"],
+                             Wd["w_o"], Wd["b_o"], h, h_out=hout, staging=staging, workspace=ws,
+                             mask=binding.make_mask(False, vld, dmd))
+    torch.cuda.synchronize()
+    ref = run_oracle(inp, valid_lens=vl, dense=dense)
+    assert_close(hout.double().numpy(), ref, "bf16")

@@ -694,6 +694,44 @@ size_t mha_host_staging_size(mha_dtype_t dt, int B, int L_q, int L_k, int d_mode
     return total;
 }
 
+}  // extern "C"
+
+namespace {
+
+// Per-device resources of the host-buffer entry point: a copy stream and events,
+// created on first use and kept for the life of the process.
+constexpr int kHostChunks = 4;
+struct HostPipe {
+    std::mutex mu;
+    bool ready = false;
+    cudaStream_t copy = nullptr;
+    cudaEvent_t start = nullptr, done = nullptr;
+    cudaEvent_t in[kHostChunks] = {}, out[kHostChunks] = {};
+};
+HostPipe g_pipes[64];
+
+mha_status_t host_pipe(int dev, HostPipe** hp) {
+    if (dev < 0 || dev >= 64) return fail(MHA_ERR_CUDA, "device ordinal %d out of range", dev);
+    HostPipe& p = g_pipes[dev];
+    if (!p.ready) {
+        cudaError_t e = cudaStreamCreateWithFlags(&p.copy, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p.start, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p.done, cudaEventDisableTiming);
+        for (int c = 0; c < kHostChunks && e == cudaSuccess; ++c) {
+            e = cudaEventCreateWithFlags(&p.in[c], cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p.out[c], cudaEventDisableTiming);
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "copy stream / event creation");
+        p.ready = true;
+    }
+    *hp = &p;
+    return MHA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 mha_status_t mha_forward_host(mha_dtype_t dt, const void* h_query, const void* h_key, const void* h_value,
                               const void* w_q, const void* b_q, const void* w_k, const void* b_k, const void* w_v,
                               const void* b_v, const void* w_o, const void* b_o, int B, int L_q, int L_k,
@@ -710,34 +748,79 @@ mha_status_t mha_forward_host(mha_dtype_t dt, const void* h_query, const void* h
     if (staging_bytes < need) return fail(MHA_ERR_INVALID_ARG, "staging too small: %zu < %zu", staging_bytes, need);
     if ((reinterpret_cast<uintptr_t>(staging) & 255u) != 0)
         return fail(MHA_ERR_INVALID_ARG, "staging not 256-byte aligned");
+    Layout L;
+    if ((st = check_workspace(dt, B, L_q, L_k, d_model, h, workspace, workspace_bytes, &L)) != MHA_OK) return st;
     const size_t es = dt == MHA_BF16 ? 2 : 4;
-    const size_t qbytes = es * B * static_cast<size_t>(L_q) * d_model;
-    const size_t kbytes = es * B * static_cast<size_t>(L_k) * d_model;
+    const size_t qrow = es * static_cast<size_t>(L_q) * d_model;   // bytes of one sequence of query / out
+    const size_t krow = es * static_cast<size_t>(L_k) * d_model;
     uint8_t* p = static_cast<uint8_t*>(staging);
     uint8_t* d_q = p;
-    p += align256(qbytes);
+    p += align256(qrow * B);
     uint8_t* d_out = p;
-    p += align256(qbytes);
+    p += align256(qrow * B);
     uint8_t* d_k = d_q;
     if (q_distinct) {
         d_k = p;
-        p += align256(kbytes);
+        p += align256(krow * B);
     }
     uint8_t* d_v = d_k;
     if (kv_distinct) {
         d_v = p;
-        p += align256(kbytes);
+        p += align256(krow * B);
     }
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    HostPipe* hp = nullptr;
+    std::lock_guard<std::mutex> lock(g_pipes[dev < 0 || dev >= 64 ? 0 : dev].mu);
+    if ((st = host_pipe(dev, &hp)) != MHA_OK) return st;
     const cudaStream_t s = as_stream(stream);
-    cudaError_t e = cudaMemcpyAsync(d_q, h_query, qbytes, cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess && q_distinct) e = cudaMemcpyAsync(d_k, h_key, kbytes, cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess && kv_distinct) e = cudaMemcpyAsync(d_v, h_value, kbytes, cudaMemcpyHostToDevice, s);
+    // Pipeline over chunks of sequences: the copy stream uploads chunk c + 1 and downloads
+    // chunk c - 1 while `stream` computes chunk c.
+    const int nch = std::min(B, kHostChunks);
+    const int per = (B + nch - 1) / nch;
+    e = cudaEventRecord(hp->start, s);   // staging / out may still be in use by earlier work on `stream`
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->copy, hp->start, 0);
+    for (int c = 0; c < nch && e == cudaSuccess; ++c) {
+        const int b0 = c * per, bc = std::min(per, B - b0);
+        if (bc <= 0) break;
+        e = cudaMemcpyAsync(d_q + qrow * b0, static_cast<const uint8_t*>(h_query) + qrow * b0, qrow * bc,
+                            cudaMemcpyHostToDevice, hp->copy);
+        if (e == cudaSuccess && q_distinct)
+            e = cudaMemcpyAsync(d_k + krow * b0, static_cast<const uint8_t*>(h_key) + krow * b0, krow * bc,
+                                cudaMemcpyHostToDevice, hp->copy);
+        if (e == cudaSuccess && kv_distinct)
+            e = cudaMemcpyAsync(d_v + krow * b0, static_cast<const uint8_t*>(h_value) + krow * b0, krow * bc,
+                                cudaMemcpyHostToDevice, hp->copy);
+        if (e == cudaSuccess) e = cudaEventRecord(hp->in[c], hp->copy);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "host to device copy");
-    st = mha_forward(dt, d_q, d_k, d_v, w_q, b_q, w_k, b_k, w_v, b_v, w_o, b_o, B, L_q, L_k, d_model, h, mask, d_out,
-                     nullptr, workspace, workspace_bytes, stream);
-    if (st != MHA_OK) return st;
-    e = cudaMemcpyAsync(h_out, d_out, qbytes, cudaMemcpyDeviceToHost, s);
-    if (e != cudaSuccess) return cuda_fail(e, "device to host copy");
+    for (int c = 0; c < nch; ++c) {
+        const int b0 = c * per, bc = std::min(per, B - b0);
+        if (bc <= 0) break;
+        if ((e = cudaStreamWaitEvent(s, hp->in[c], 0)) != cudaSuccess) return cuda_fail(e, "stream wait");
+        mha_mask_t mc;
+        const mha_mask_t* mp = nullptr;
+        if (mask) {
+            mc = *mask;
+            if (mc.key_valid_lens) mc.key_valid_lens += b0;
+            if (mc.dense) mc.dense += static_cast<size_t>(b0) * mc.dense_mq * L_k;
+            mp = &mc;
+        }
+        st = mha_forward(dt, d_q + qrow * b0, d_k + krow * b0, d_v + krow * b0, w_q, b_q, w_k, b_k, w_v, b_v, w_o,
+                         b_o, bc, L_q, L_k, d_model, h, mp, d_out + qrow * b0, nullptr, workspace, workspace_bytes,
+                         stream);
+        if (st != MHA_OK) return st;
+        e = cudaEventRecord(hp->out[c], s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->copy, hp->out[c], 0);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(static_cast<uint8_t*>(h_out) + qrow * b0, d_out + qrow * b0, qrow * bc,
+                                cudaMemcpyDeviceToHost, hp->copy);
+        if (e != cudaSuccess) return cuda_fail(e, "device to host copy");
+    }
+    e = cudaEventRecord(hp->done, hp->copy);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hp->done, 0);   // `stream` covers the whole call
+    if (e != cudaSuccess) return cuda_fail(e, "stream wait");
     return MHA_OK;
 }
 
