@@ -176,68 +176,84 @@ def job_throughput(world: int, flops_per_rank: float, ms_per_step: float) -> flo
     return world * flops_per_rank / (ms_per_step * 1e-3) / 1e12
 
 
+def oracle_sample(workload: str, prefix: int):
+    """A bounded, complete sub-problem of ``workload`` for the fp64 oracle.
+
+    Long sequences: one sequence's causal prefix of ``prefix`` tokens (rows
+    0..P-1 of a causal output depend only on tokens 0..P-1). Short ones: the
+    first sequence of the batch, whole, with its own mask. Returns
+    (run, flops, tokens, description)."""
+    import oracle
+    from transformer_head_scaled_fwd_gb300 import workloads as W
+    oracle.build()
+    wl = W.WORKLOADS[workload]
+    inp = W.make_inputs(wl, B=1)
+    w = inp.weights
+    if wl.Lq > prefix:
+        assert wl.causal and wl.self_attn
+        x = np.ascontiguousarray(inp.query[:, :prefix])
+        q = k = v = x
+        Lq = Lk = prefix
+        vl = None
+        desc = f"1 sequence, causal prefix of {prefix} tokens"
+    else:
+        q = np.ascontiguousarray(inp.query)
+        k = q if inp.key is inp.query else np.ascontiguousarray(inp.key)
+        v = k
+        Lq, Lk = q.shape[1], k.shape[1]
+        vl = None if inp.valid_lens is None else np.ascontiguousarray(inp.valid_lens[:1])
+        desc = f"1 whole sequence (L_q {Lq}, L_k {Lk}) with its mask"
+    proj, attn = algorithmic_flops(1, Lq, Lk, wl.d_model, wl.h, wl.causal, vl)
+
+    def run():
+        oracle.mha_forward(q, k, v, w["w_q"], w["b_q"], w["w_k"], w["b_k"], w["w_v"], w["b_v"], w["w_o"],
+                           w["b_o"], wl.h, causal=wl.causal, valid_lens=vl)
+
+    desc += f" of the workload (d_model {wl.d_model}, h {wl.h}), fp64 C oracle, OpenMP"
+    return run, proj + attn, Lq, desc
+
+
 def run_reference(args):
-    """The fp64 oracle on the host cores, on a bounded causal-prefix sample of the workload."""
+    """The fp64 oracle on the host cores, on a bounded sample of the workload."""
     world, rank, _ = dist_setup()
     if rank != 0:
         return
     import oracle
-    from transformer_head_scaled_fwd_gb300 import workloads as W
-    oracle.build()
-    wl = W.WORKLOADS[WORKLOAD]
-    P = args.ref_prefix
-    inp = W.make_inputs(wl, B=1)
-    # A causal prefix of one sequence is a complete problem of its own: rows
-    # 0..P-1 of the full output depend only on tokens 0..P-1.
-    x = np.ascontiguousarray(inp.query[:, :P])
-    w = inp.weights
-    proj, attn = algorithmic_flops(1, P, P, wl.d_model, wl.h, True)
+    run, flops, tokens, sample = oracle_sample(args.workload, args.ref_prefix)
     times = []
     for s in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        oracle.mha_forward(x, x, x, w["w_q"], w["b_q"], w["w_k"], w["b_k"], w["w_v"], w["b_v"], w["w_o"],
-                           w["b_o"], wl.h, causal=True)
+        run()
         dt = time.perf_counter() - t0
         if s >= args.warmup:
             times.append(dt)
     mean = sum(times) / len(times)
-    value = (proj + attn) / mean / 1e12
+    value = flops / mean / 1e12
     cores = oracle.num_threads()
-    sample = f"1 sequence, causal prefix of {P} tokens (d_model 1024, h 16), fp64, OpenMP"
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "long-sequence causal self-attention B4 L8192 d_model1024 h16 d_k64 (oracle sample)",
-                   "B": 1, "seq_len": P, "d_model": wl.d_model, "h": wl.h, "causal": True},
-        "tokens_per_s": P / mean,
+        "config": {"workload": DESCRIPTION[args.workload] + " (oracle sample)", "sample": sample},
+        "tokens_per_s": tokens / mean,
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-def cpu_baseline(prefix: int):
+def cpu_baseline(workload: str, prefix: int):
     import oracle
-    from transformer_head_scaled_fwd_gb300 import workloads as W
-    oracle.build()
-    wl = W.WORKLOADS[WORKLOAD]
-    inp = W.make_inputs(wl, B=1)
-    x = np.ascontiguousarray(inp.query[:, :prefix])
-    w = inp.weights
-    proj, attn = algorithmic_flops(1, prefix, prefix, wl.d_model, wl.h, True)
+    run, flops, _, sample = oracle_sample(workload, prefix)
     runs, t0 = 0, time.perf_counter()
     while True:   # about 10 s of CPU work: repeat the sample
-        oracle.mha_forward(x, x, x, w["w_q"], w["b_q"], w["w_k"], w["b_k"], w["w_v"], w["b_v"], w["w_o"],
-                           w["b_o"], wl.h, causal=True)
+        run()
         runs += 1
         dt = time.perf_counter() - t0
         if dt >= 10.0 or runs >= 30:
             break
-    return {"value": runs * (proj + attn) / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
-            "kind": "oracle", "seconds": dt,
-            "sample": f"{runs} runs of 1 sequence, causal prefix of {prefix} tokens of the workload "
-                      f"(d_model 1024, h 16), fp64 C oracle, OpenMP"}
+    return {"value": runs * flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds": dt, "sample": f"{runs} runs of {sample}"}
 
 
 def run_gpu(args):
@@ -259,7 +275,7 @@ def run_gpu(args):
     # CPU baseline first (rank 0, N=1 only), before any GPU work is timed.
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(args.ref_prefix)
+        cpu = cpu_baseline(args.workload, args.ref_prefix)
 
     wl = W.WORKLOADS[args.workload]
     # weak scaling: every rank runs the full per-GPU batch with its own seed
@@ -282,13 +298,16 @@ def run_gpu(args):
     proj, attn = algorithmic_flops(Bn, Lq, Lk, d, h, wl.causal, inp.valid_lens)
     flops = proj + attn
 
-    def step():
+    def step(st=None, marks=None):
+        st = stream if st is None else st
         binding.mha_qkv_projection(q, k, v, Wt["w_q"], Wt["b_q"], Wt["w_k"], Wt["b_k"], Wt["w_v"], Wt["b_v"], h,
-                                   workspace=ws, stream=stream)
-        ev[1].record(stream)
-        binding.mha_attention_core(binding.MHA_BF16, Bn, Lq, Lk, d, h, workspace=ws, mask=mask, stream=stream)
-        ev[2].record(stream)
-        binding.mha_output_projection(Wt["w_o"], Wt["b_o"], Bn, Lq, Lk, h, out=out, workspace=ws, stream=stream)
+                                   workspace=ws, stream=st)
+        if marks is not None:
+            marks[1].record(st)
+        binding.mha_attention_core(binding.MHA_BF16, Bn, Lq, Lk, d, h, workspace=ws, mask=mask, stream=st)
+        if marks is not None:
+            marks[2].record(st)
+        binding.mha_output_projection(Wt["w_o"], Wt["b_o"], Bn, Lq, Lk, h, out=out, workspace=ws, stream=st)
 
     K, Wm = args.steps, args.warmup
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K + Wm)]
@@ -317,10 +336,22 @@ def run_gpu(args):
         ev = evs[s]
         flush.zero_()
         ev[0].record(stream)
-        step()
+        step(marks=ev)
         ev[3].record(stream)
         e2e_step(s)
     torch.cuda.synchronize()
+
+    # ---- the same three launches captured once in a CUDA graph (replayed below)
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step(st=torch.cuda.current_stream())
+        for s in range(Wm):
+            flush.zero_()
+            graph.replay()
+        torch.cuda.synchronize()
+    g_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
 
     launches = 0
     with ClockSampler(local) as clk:
@@ -332,7 +363,7 @@ def run_gpu(args):
             ev = evs[s]
             flush.zero_()                      # evict L2 between steps (outside the events)
             ev[0].record(stream)
-            step()
+            step(marks=ev)
             ev[3].record(stream)
             launches += 3
         torch.cuda.synchronize()
@@ -344,6 +375,16 @@ def run_gpu(args):
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
+        if graph is not None:
+            for s in range(K):
+                flush.zero_()
+                g_ev[s][0].record(stream)
+                graph.replay()
+                g_ev[s][1].record(stream)
+                launches += 3
+            torch.cuda.synchronize()
+            if world > 1:
+                dist.barrier()
     status = binding.mha_check_device_status(reset=True)
     if status != 0:
         raise RuntimeError(f"a pipeline wait gave up inside a kernel (status 0x{status:x})")
@@ -359,6 +400,21 @@ def run_gpu(args):
     e2e_ms = e2e_total / K
     e2e_value = job_throughput(world, flops, e2e_ms)
 
+    graph_line = None
+    if graph is not None:
+        g_ms = [a.elapsed_time(b) for a, b in g_ev]
+        g_total, _ = job_times(sum(g_ms), 0.0, world, device="cuda")
+        graph_line = {"ms_per_step": g_total / K, "median_ms_per_step": statistics.median(g_ms),
+                      "value": job_throughput(world, flops, g_total / K), "unit": "TFLOP/s",
+                      "note": "the step's three launches captured once in a CUDA graph, replayed; L2 flushed between replays"}
+    # attention core alone: compute rate and algorithmic bytes (Q, K, V read once, ctx written, bf16)
+    core_bytes = 2 * (Bn * Lq * d + 2 * Bn * Lk * d + Bn * Lq * d)
+    att_mean = statistics.mean(att_ms)
+    core = {"ms": att_mean, "median_ms": statistics.median(att_ms), "tflops": attn / (att_mean * 1e-3) / 1e12,
+            "algorithmic_bytes": core_bytes, "gbs": core_bytes / (att_mean * 1e-3) / 1e9,
+            "hbm_frac": core_bytes / (att_mean * 1e-3) / 1e9 / float(peaks["hbm_gbs"]),
+            "bf16_frac": attn / (att_mean * 1e-3) / 1e12 / float(peaks["bf16_tflops"])}
+
     # ---- roofline of the dominant kernel (largest share of the step)
     shares = {"qkv_projection_gemm": statistics.mean(qkv_ms), "attention_core": statistics.mean(att_ms),
               "output_projection_gemm": statistics.mean(out_ms)}
@@ -370,7 +426,8 @@ def run_gpu(args):
     traffic = committed_traffic(dom, args.workload)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": Wm,
-        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "ms_per_step": ms_per_step, "median_ms_per_step": statistics.median(step_ms),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded N(0,1) activations, Xavier-uniform weights)",
         "config": {"workload": DESCRIPTION[args.workload],
                    "B_per_gpu": Bn, "global_batch": Bn * world, "seq_len": Lq, "d_model": d, "h": h,
@@ -380,6 +437,8 @@ def run_gpu(args):
         "tokens_per_s": world * Bn * Lq / (ms_per_step * 1e-3),
         "pct_of_bf16_peak": 100.0 * value / peak,
         "stage_ms": {k2: round(v2, 4) for k2, v2 in shares.items()},
+        "attention_core": core,
+        "graph": graph_line,
         "roofline": {"kernel": dom, "source_sha1": source_digest(dom), "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_src} bf16_tflops (burst); sustained {peaks.get('bf16_tflops_sustained')}"},
@@ -579,6 +638,7 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD, choices=["enc", "dec", "xattn", "long", "long_d128"])
     ap.add_argument("--ref-prefix", type=int, default=2048, help="causal prefix length of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA graph replay variant")
     ap.add_argument("--decode-batch", type=int, default=16)
     ap.add_argument("--decode-context", type=int, default=8192)
     ap.add_argument("--path", choices=["mha", "ffn", "sublayer", "decode"], default="mha",
