@@ -256,6 +256,17 @@ def cpu_baseline(workload: str, prefix: int):
             "kind": "oracle", "seconds": dt, "sample": f"{runs} runs of {sample}"}
 
 
+def host_pipeline_launches(B: int, L_q: int, L_k: int, self_attn: bool) -> int:
+    """Library kernels one bf16 mha_forward_host call launches: 3 per chunk of sequences
+    (up to 4 chunks), plus one more projection at each end when query, key and value are one
+    host buffer (the first chunk's Q/K/V projection and the last chunk's output projection
+    each run in 2 row windows; one chunk holds both ends when B = 1)."""
+    n = 3 * min(B, 4)
+    if self_attn and L_q == L_k and L_q >= 256:
+        n += 2
+    return n
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -369,9 +380,10 @@ def run_gpu(args):
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
+        per_e2e = host_pipeline_launches(Bn, Lq, Lk, inp.key is inp.query and inp.value is inp.key)
         for s in range(Wm, Wm + K):
             e2e_step(s)
-            launches += 3
+            launches += per_e2e
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()

@@ -145,12 +145,19 @@ mha_status_t mha_output_projection(mha_dtype_t dt, const void* w_o, const void* 
  * above. The host buffers should be page-locked for the copies to be
  * asynchronous. `staging` is device memory of at least
  * mha_host_staging_size(...) bytes that receives the activations. The call is
- * pipelined over up to 4 chunks of sequences: a library-owned copy stream (one
- * per device, created on first use) uploads chunk c+1 and downloads chunk c-1
- * while `stream` computes chunk c (host->device copies of query, and of key
- * and value unless they alias query / each other; the three stages; the
- * device->host copy of out), ordered by events. When the call returns, all of
- * it is enqueued behind `stream`: synchronise `stream` before reading out.
+ * pipelined over up to 4 chunks of sequences with library-owned streams (one set
+ * per device, created on first use): an upload stream, a download stream and a
+ * second compute stream. Chunks alternate between `stream` and the second
+ * compute stream when the workspace holds two chunk workspaces (each
+ * mha_workspace_size(dt, ceil(B / chunks), ...) bytes; true whenever B >= 2 at
+ * realistic sizes), otherwise all run on `stream`. When query, key and value
+ * are the same host buffer (bf16, L >= 256), the first chunk is uploaded and
+ * projected in two row windows and the last chunk's output projection and
+ * download run in two row windows. Copies: host->device of query (and of key and value unless they
+ * alias query / each other), device->host of out; all ordered by events. When
+ * the call returns, all of it is enqueued behind `stream`: synchronise `stream`
+ * before reading out. The workspace must not be used by other work on other
+ * streams while the call runs.
  */
 size_t mha_host_staging_size(mha_dtype_t dt, int B, int L_q, int L_k, int d_model,
                              int kv_distinct, int q_distinct);

@@ -127,7 +127,8 @@ def _stream(stream):
 
 
 def make_mask(causal=False, key_valid_lens=None, dense=None):
-    """Build the C mask struct (keep the tensors alive while the call runs)."""
+    """Build the C mask struct. The struct holds references to the two tensors, so
+    they stay allocated for as long as the struct is alive."""
     if not causal and key_valid_lens is None and dense is None:
         return None
     m = MaskT()
@@ -135,6 +136,7 @@ def make_mask(causal=False, key_valid_lens=None, dense=None):
     m.key_valid_lens = _ptr(key_valid_lens)
     m.dense = _ptr(dense)
     m.dense_mq = int(dense.shape[1]) if dense is not None else 0
+    m._tensors = (key_valid_lens, dense)
     return m
 
 

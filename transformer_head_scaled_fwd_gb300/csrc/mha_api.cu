@@ -84,10 +84,11 @@ mha_status_t encode_bf16(CUtensorMap* m, const void* base, int rank, const uint6
     return MHA_OK;
 }
 
-// [B, L, N] row-major bf16 as {N, L, B}, box {64, 128, 1}
-mha_status_t map_rows(CUtensorMap* m, const void* base, int B, int L, int N, const char* what) {
+// [B, L_stride, N] row-major bf16, first L rows of each sequence, as {N, L, B}, box {64, 128, 1}
+mha_status_t map_rows(CUtensorMap* m, const void* base, int B, int L, int N, const char* what, int L_stride = 0) {
+    if (L_stride <= 0) L_stride = L;
     const uint64_t dims[3] = {(uint64_t)N, (uint64_t)L, (uint64_t)B};
-    const uint64_t str[2] = {(uint64_t)N * 2, (uint64_t)L * N * 2};
+    const uint64_t str[2] = {(uint64_t)N * 2, (uint64_t)L_stride * N * 2};
     const uint32_t box[3] = {64, 128, 1};
     return encode_bf16(m, base, 3, dims, str, box, what);
 }
@@ -170,6 +171,20 @@ mha_status_t check_mask(const mha_mask_t* mask, int Lq, int Lk) {
 
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
+
+// Stage implementations without argument checks (defined below). A row window
+// [r0, r0 + rows) (rows > 0) restricts a projection to those sequence rows of the
+// full-length tensors.
+mha_status_t qkv_bf16_impl(const void* query, const void* key, const void* value, const void* w_q, const void* b_q,
+                           const void* w_k, const void* b_k, const void* w_v, const void* b_v, int B, int L_q,
+                           int L_k, int d_model, int h, const Layout& L, uint8_t* ws, cudaStream_t s, int r0,
+                           int rows);
+mha_status_t attention_impl(mha_dtype_t dt, int B, int L_q, int L_k, int d_model, int h, const mha_mask_t* mask,
+                            float* p_attn, const Layout& L, uint8_t* ws, cudaStream_t s);
+mha_status_t output_projection_impl(mha_dtype_t dt, const void* w_o, const void* b_o, const void* residual,
+                                    int B, int L_q, int d_model, int h, void* out, const Layout& L, uint8_t* ws,
+                                    cudaStream_t s, int r0 = 0, int rows = 0);
+
 }  // namespace
 
 void mha::set_last_error(const char* msg) { g_last_error = msg; }
@@ -245,21 +260,43 @@ mha_status_t mha_qkv_projection(mha_dtype_t dt, const void* query, const void* k
     const void* ptrs[9] = {query, key, value, w_q, w_k, w_v, b_q, b_k, b_v};
     for (const void* ptr : ptrs)
         if (ptr && !aligned16(ptr)) return fail(MHA_ERR_INVALID_ARG, "bf16 tensors must be 16-byte aligned");
+    return qkv_bf16_impl(query, key, value, w_q, b_q, w_k, b_k, w_v, b_v, B, L_q, L_k, d_model, h, L, ws, s, 0, 0);
+}
+
+}  // extern "C"
+
+namespace {
+
+// bf16 Q/K/V projections into the workspace's head-split tensors; no argument checks.
+// rows > 0 restricts all three to the sequence rows [r0, r0 + rows) (self-attention,
+// L_q == L_k): the maps address that window of the full-length tensors.
+mha_status_t qkv_bf16_impl(const void* query, const void* key, const void* value, const void* w_q, const void* b_q,
+                           const void* w_k, const void* b_k, const void* w_v, const void* b_v, int B, int L_q,
+                           int L_k, int d_model, int h, const Layout& L, uint8_t* ws, cudaStream_t s, int r0,
+                           int rows) {
+    const int dk = d_model / h;
+    mha_status_t st;
     if ((st = get_encoder()) != MHA_OK) return st;
     mha::GemmParams p;
     memset(&p, 0, sizeof(p));
     const void* A[3] = {query, key, value};
     const void* W[3] = {w_q, w_k, w_v};
     const void* bias[3] = {b_q, b_k, b_v};
-    const int Ls[3] = {L_q, L_k, L_k};
+    const int Lfull[3] = {L_q, L_k, L_k};
+    const int Ls[3] = {rows > 0 ? rows : L_q, rows > 0 ? rows : L_k, rows > 0 ? rows : L_k};
+    const size_t in_off = static_cast<size_t>(r0) * d_model * 2;    // window start in an input row block
+    const size_t out_off = static_cast<size_t>(r0) * dk * 2;        // ... in a head plane
     int max_m = 0;
     for (int g = 0; g < 3; ++g) {
-        if ((st = map_rows(&p.a[g], A[g], B, Ls[g], d_model, "projection input")) != MHA_OK) return st;
+        if ((st = map_rows(&p.a[g], static_cast<const uint8_t*>(A[g]) + in_off, B, Ls[g], d_model,
+                           "projection input", Lfull[g])) != MHA_OK)
+            return st;
         if ((st = map_weight(&p.w[g], W[g], d_model, d_model)) != MHA_OK) return st;
         if (g == 0) {
-            if ((st = map_heads5(&p.out[g], ws + L.q, B, h, L_q, dk / 64)) != MHA_OK) return st;
+            if ((st = map_heads5(&p.out[g], ws + L.q + out_off, B, h, Ls[g], dk / 64, L_q)) != MHA_OK) return st;
         } else {
-            if ((st = map_heads5(&p.out[g], ws + L.kv, B, 2 * h, L_k, dk / 64)) != MHA_OK) return st;
+            if ((st = map_heads5(&p.out[g], ws + L.kv + out_off, B, 2 * h, Ls[g], dk / 64, L_k)) != MHA_OK)
+                return st;
         }
         p.g[g].L = Ls[g];
         p.g[g].tiles_per_b = (Ls[g] + mha::kGemmBM - 1) / mha::kGemmBM;
@@ -280,6 +317,10 @@ mha_status_t mha_qkv_projection(mha_dtype_t dt, const void* query, const void* k
     return MHA_OK;
 }
 
+}  // namespace
+
+extern "C" {
+
 mha_status_t mha_attention_core(mha_dtype_t dt, int B, int L_q, int L_k, int d_model, int h,
                                 const mha_mask_t* mask, float* p_attn, void* workspace, size_t workspace_bytes,
                                 void* stream) {
@@ -288,9 +329,18 @@ mha_status_t mha_attention_core(mha_dtype_t dt, int B, int L_q, int L_k, int d_m
     if ((st = check_mask(mask, L_q, L_k)) != MHA_OK) return st;
     Layout L;
     if ((st = check_workspace(dt, B, L_q, L_k, d_model, h, workspace, workspace_bytes, &L)) != MHA_OK) return st;
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    return attention_impl(dt, B, L_q, L_k, d_model, h, mask, p_attn, L, static_cast<uint8_t*>(workspace),
+                          as_stream(stream));
+}
+
+}  // extern "C"
+
+namespace {
+
+mha_status_t attention_impl(mha_dtype_t dt, int B, int L_q, int L_k, int d_model, int h, const mha_mask_t* mask,
+                            float* p_attn, const Layout& L, uint8_t* ws, cudaStream_t s) {
+    mha_status_t st;
     const int dk = d_model / h;
-    const cudaStream_t s = as_stream(stream);
     const int causal = mask ? (mask->causal != 0) : 0;
     const int32_t* vl = mask ? mask->key_valid_lens : nullptr;
     const uint8_t* dense = mask ? mask->dense : nullptr;
@@ -346,14 +396,10 @@ mha_status_t mha_attention_core(mha_dtype_t dt, int B, int L_q, int L_k, int d_m
     return MHA_OK;
 }
 
-}  // extern "C"
-
-namespace {
-
 // out = ctx W_o^T + b_o (+ residual), reading ctx from the workspace; no argument checks.
 mha_status_t output_projection_impl(mha_dtype_t dt, const void* w_o, const void* b_o, const void* residual,
                                     int B, int L_q, int d_model, int h, void* out, const Layout& L, uint8_t* ws,
-                                    cudaStream_t s) {
+                                    cudaStream_t s, int r0, int rows) {
     if (dt == MHA_F32) {
         mha::F32GemmParams p{};
         p.ngroups = 1;
@@ -372,11 +418,16 @@ mha_status_t output_projection_impl(mha_dtype_t dt, const void* w_o, const void*
     if (st != MHA_OK) return st;
     mha::GemmParams p;
     memset(&p, 0, sizeof(p));
-    if ((st = map_rows(&p.a[0], ws + L.ctx, B, L_q, d_model, "context")) != MHA_OK) return st;
+    const int Lw = rows > 0 ? rows : L_q;
+    const size_t off = static_cast<size_t>(r0) * d_model * 2;
+    if ((st = map_rows(&p.a[0], ws + L.ctx + off, B, Lw, d_model, "context", L_q)) != MHA_OK) return st;
     if ((st = map_weight(&p.w[0], w_o, d_model, d_model)) != MHA_OK) return st;
-    if ((st = map_rows(&p.out[0], out, B, L_q, d_model, "output")) != MHA_OK) return st;
-    p.g[0].L = L_q;
-    p.g[0].tiles_per_b = (L_q + mha::kGemmBM - 1) / mha::kGemmBM;
+    if ((st = map_rows(&p.out[0], static_cast<uint8_t*>(out) + off, B, Lw, d_model, "output", L_q)) != MHA_OK)
+        return st;
+    if (residual && rows > 0)   // the epilogue indexes the residual with the window's own row count
+        return fail(MHA_ERR_UNSUPPORTED, "row-window output projection takes no residual");
+    p.g[0].L = Lw;
+    p.g[0].tiles_per_b = (Lw + mha::kGemmBM - 1) / mha::kGemmBM;
     p.g[0].m_tiles = B * p.g[0].tiles_per_b;
     p.g[0].bias = static_cast<const __nv_bfloat16*>(b_o);
     p.g[0].residual = static_cast<const __nv_bfloat16*>(residual);
@@ -698,15 +749,18 @@ size_t mha_host_staging_size(mha_dtype_t dt, int B, int L_q, int L_k, int d_mode
 
 namespace {
 
-// Per-device resources of the host-buffer entry point: a copy stream and events,
-// created on first use and kept for the life of the process.
+// Per-device resources of the host-buffer entry point: an upload stream, a
+// download stream, a second compute stream and events, created on first use
+// and kept for the life of the process.
 constexpr int kHostChunks = 4;
+constexpr int kHostWindows = 2;   // row windows of the first and the last chunk (self-attention)
+constexpr int kHostUnits = kHostChunks + 2 * kHostWindows;
 struct HostPipe {
     std::mutex mu;
     bool ready = false;
-    cudaStream_t copy = nullptr;
+    cudaStream_t h2d = nullptr, d2h = nullptr, compute2 = nullptr;
     cudaEvent_t start = nullptr, done = nullptr;
-    cudaEvent_t in[kHostChunks] = {}, out[kHostChunks] = {};
+    cudaEvent_t in[kHostUnits] = {}, comp[kHostUnits] = {};
 };
 HostPipe g_pipes[64];
 
@@ -714,12 +768,14 @@ mha_status_t host_pipe(int dev, HostPipe** hp) {
     if (dev < 0 || dev >= 64) return fail(MHA_ERR_CUDA, "device ordinal %d out of range", dev);
     HostPipe& p = g_pipes[dev];
     if (!p.ready) {
-        cudaError_t e = cudaStreamCreateWithFlags(&p.copy, cudaStreamNonBlocking);
+        cudaError_t e = cudaStreamCreateWithFlags(&p.h2d, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p.d2h, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p.compute2, cudaStreamNonBlocking);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p.start, cudaEventDisableTiming);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p.done, cudaEventDisableTiming);
-        for (int c = 0; c < kHostChunks && e == cudaSuccess; ++c) {
+        for (int c = 0; c < kHostUnits && e == cudaSuccess; ++c) {
             e = cudaEventCreateWithFlags(&p.in[c], cudaEventDisableTiming);
-            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p.out[c], cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p.comp[c], cudaEventDisableTiming);
         }
         if (e != cudaSuccess) return cuda_fail(e, "copy stream / event creation");
         p.ready = true;
@@ -775,30 +831,71 @@ mha_status_t mha_forward_host(mha_dtype_t dt, const void* h_query, const void* h
     std::lock_guard<std::mutex> lock(g_pipes[dev < 0 || dev >= 64 ? 0 : dev].mu);
     if ((st = host_pipe(dev, &hp)) != MHA_OK) return st;
     const cudaStream_t s = as_stream(stream);
-    // Pipeline over chunks of sequences: the copy stream uploads chunk c + 1 and downloads
-    // chunk c - 1 while `stream` computes chunk c.
+    // Pipeline over chunks of sequences: uploads on one library stream, downloads on
+    // another, and the chunks' compute alternating between `stream` and a second
+    // library stream (each with its own part of the workspace), so that one chunk's
+    // kernels fill the SMs the previous chunk's last waves leave idle. For
+    // self-attention (one tensor as query, key and value) the two exposed ends are cut
+    // into row windows: the first chunk is uploaded window by window and each window's
+    // Q/K/V projection starts as soon as its rows have arrived, and the last chunk's
+    // output projection and download run window by window after its attention.
     const int nch = std::min(B, kHostChunks);
     const int per = (B + nch - 1) / nch;
-    e = cudaEventRecord(hp->start, s);   // staging / out may still be in use by earlier work on `stream`
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->copy, hp->start, 0);
+    Layout Lc;
+    layout_of(dt, per, L_q, L_k, d_model, h, &Lc);
+    const bool two = nch >= 2 && 2 * Lc.total <= workspace_bytes;
+    uint8_t* ws_of[2] = {static_cast<uint8_t*>(workspace), static_cast<uint8_t*>(workspace) + Lc.total};
+    const size_t ws_bytes = two ? Lc.total : workspace_bytes;
+    constexpr int kWinRows = mha::kGemmBM;   // window boundaries on whole GEMM row tiles
+    const bool split = dt == MHA_BF16 && !q_distinct && !kv_distinct && L_q == L_k &&
+                       L_q >= kHostWindows * kWinRows;
+    const int nwin = split ? kHostWindows : 1;
+    int wr[kHostWindows + 1];
+    wr[0] = 0;
+    for (int w = 1; w < nwin; ++w) wr[w] = static_cast<int>(static_cast<long>(L_q) * w / nwin / kWinRows) * kWinRows;
+    wr[nwin] = L_q;
+    if (split) {   // the stages run without mha_forward's own checks
+        const void* ptrs[8] = {w_q, w_k, w_v, w_o, b_q, b_k, b_v, b_o};
+        for (const void* ptr : ptrs)
+            if (ptr && !aligned16(ptr)) return fail(MHA_ERR_INVALID_ARG, "bf16 tensors must be 16-byte aligned");
+        if (!w_q || !w_k || !w_v || !w_o) return fail(MHA_ERR_INVALID_ARG, "W_q, W_k, W_v and W_o must not be NULL");
+    }
+    const size_t rowq = es * static_cast<size_t>(d_model);   // bytes of one token row
+    // windows of chunk c on the input side (its upload + projection) and the output side
+    auto in_windows = [&](int c) { return (split && c == 0) ? nwin : 1; };
+    auto out_windows = [&](int c) { return (split && c == nch - 1) ? nwin : 1; };
+    auto win_lo = [&](int n, int w) { return n == 1 ? 0 : wr[w]; };
+    auto win_hi = [&](int n, int w) { return n == 1 ? L_q : wr[w + 1]; };
+    e = cudaEventRecord(hp->start, s);   // staging / out / workspace may still be in use by earlier work on `stream`
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->h2d, hp->start, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->d2h, hp->start, 0);
+    if (e == cudaSuccess && two) e = cudaStreamWaitEvent(hp->compute2, hp->start, 0);
+    int n_in = 0;
     for (int c = 0; c < nch && e == cudaSuccess; ++c) {
         const int b0 = c * per, bc = std::min(per, B - b0);
         if (bc <= 0) break;
-        e = cudaMemcpyAsync(d_q + qrow * b0, static_cast<const uint8_t*>(h_query) + qrow * b0, qrow * bc,
-                            cudaMemcpyHostToDevice, hp->copy);
-        if (e == cudaSuccess && q_distinct)
-            e = cudaMemcpyAsync(d_k + krow * b0, static_cast<const uint8_t*>(h_key) + krow * b0, krow * bc,
-                                cudaMemcpyHostToDevice, hp->copy);
-        if (e == cudaSuccess && kv_distinct)
-            e = cudaMemcpyAsync(d_v + krow * b0, static_cast<const uint8_t*>(h_value) + krow * b0, krow * bc,
-                                cudaMemcpyHostToDevice, hp->copy);
-        if (e == cudaSuccess) e = cudaEventRecord(hp->in[c], hp->copy);
+        const int nw = in_windows(c);
+        for (int w = 0; w < nw && e == cudaSuccess; ++w) {
+            const int r0 = win_lo(nw, w), r1 = win_hi(nw, w);
+            const size_t off = qrow * b0 + rowq * r0;
+            e = cudaMemcpy2DAsync(d_q + off, qrow, static_cast<const uint8_t*>(h_query) + off, qrow,
+                                  rowq * (r1 - r0), bc, cudaMemcpyHostToDevice, hp->h2d);
+            if (e == cudaSuccess && q_distinct)
+                e = cudaMemcpyAsync(d_k + krow * b0, static_cast<const uint8_t*>(h_key) + krow * b0, krow * bc,
+                                    cudaMemcpyHostToDevice, hp->h2d);
+            if (e == cudaSuccess && kv_distinct)
+                e = cudaMemcpyAsync(d_v + krow * b0, static_cast<const uint8_t*>(h_value) + krow * b0, krow * bc,
+                                    cudaMemcpyHostToDevice, hp->h2d);
+            if (e == cudaSuccess) e = cudaEventRecord(hp->in[n_in++], hp->h2d);
+        }
     }
     if (e != cudaSuccess) return cuda_fail(e, "host to device copy");
+    int n_in_used = 0, n_out = 0;
     for (int c = 0; c < nch; ++c) {
         const int b0 = c * per, bc = std::min(per, B - b0);
         if (bc <= 0) break;
-        if ((e = cudaStreamWaitEvent(s, hp->in[c], 0)) != cudaSuccess) return cuda_fail(e, "stream wait");
+        const int lane = two ? (c & 1) : 0;
+        const cudaStream_t sc = lane ? hp->compute2 : s;
         mha_mask_t mc;
         const mha_mask_t* mp = nullptr;
         if (mask) {
@@ -807,19 +904,51 @@ mha_status_t mha_forward_host(mha_dtype_t dt, const void* h_query, const void* h
             if (mc.dense) mc.dense += static_cast<size_t>(b0) * mc.dense_mq * L_k;
             mp = &mc;
         }
-        st = mha_forward(dt, d_q + qrow * b0, d_k + krow * b0, d_v + krow * b0, w_q, b_q, w_k, b_k, w_v, b_v, w_o,
-                         b_o, bc, L_q, L_k, d_model, h, mp, d_out + qrow * b0, nullptr, workspace, workspace_bytes,
-                         stream);
-        if (st != MHA_OK) return st;
-        e = cudaEventRecord(hp->out[c], s);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->copy, hp->out[c], 0);
-        if (e == cudaSuccess)
-            e = cudaMemcpyAsync(static_cast<uint8_t*>(h_out) + qrow * b0, d_out + qrow * b0, qrow * bc,
-                                cudaMemcpyDeviceToHost, hp->copy);
-        if (e != cudaSuccess) return cuda_fail(e, "device to host copy");
+        Layout Lb;
+        layout_of(dt, bc, L_q, L_k, d_model, h, &Lb);
+        const int nwi = in_windows(c), nwo = out_windows(c);
+        if (split) {
+            uint8_t* xq = d_q + qrow * b0;
+            for (int w = 0; w < nwi; ++w) {
+                if ((e = cudaStreamWaitEvent(sc, hp->in[n_in_used++], 0)) != cudaSuccess)
+                    return cuda_fail(e, "stream wait");
+                const int r0 = win_lo(nwi, w), r1 = win_hi(nwi, w);
+                if ((st = qkv_bf16_impl(xq, xq, xq, w_q, b_q, w_k, b_k, w_v, b_v, bc, L_q, L_k, d_model, h, Lb,
+                                        ws_of[lane], sc, r0, nwi == 1 ? 0 : r1 - r0)) != MHA_OK)
+                    return st;
+            }
+            if ((st = attention_impl(dt, bc, L_q, L_k, d_model, h, mp, nullptr, Lb, ws_of[lane], sc)) != MHA_OK)
+                return st;
+        } else {
+            if ((e = cudaStreamWaitEvent(sc, hp->in[n_in_used++], 0)) != cudaSuccess)
+                return cuda_fail(e, "stream wait");
+        }
+        for (int w = 0; w < nwo; ++w) {
+            const int r0 = win_lo(nwo, w), r1 = win_hi(nwo, w);
+            if (split) {
+                if ((st = output_projection_impl(dt, w_o, b_o, nullptr, bc, L_q, d_model, h, d_out + qrow * b0, Lb,
+                                                 ws_of[lane], sc, r0, nwo == 1 ? 0 : r1 - r0)) != MHA_OK)
+                    return st;
+            } else {
+                st = mha_forward(dt, d_q + qrow * b0, d_k + krow * b0, d_v + krow * b0, w_q, b_q, w_k, b_k, w_v, b_v,
+                                 w_o, b_o, bc, L_q, L_k, d_model, h, mp, d_out + qrow * b0, nullptr, ws_of[lane],
+                                 ws_bytes, sc);
+                if (st != MHA_OK) return st;
+            }
+            const int u = n_out++;
+            e = cudaEventRecord(hp->comp[u], sc);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->d2h, hp->comp[u], 0);
+            if (e == cudaSuccess) {
+                const size_t off = qrow * b0 + rowq * r0;
+                e = cudaMemcpy2DAsync(static_cast<uint8_t*>(h_out) + off, qrow, d_out + off, qrow, rowq * (r1 - r0),
+                                      bc, cudaMemcpyDeviceToHost, hp->d2h);
+            }
+            if (e != cudaSuccess) return cuda_fail(e, "device to host copy");
+        }
     }
-    e = cudaEventRecord(hp->done, hp->copy);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hp->done, 0);   // `stream` covers the whole call
+    // Every chunk's compute precedes its download, so `done` covers all of the call.
+    e = cudaEventRecord(hp->done, hp->d2h);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hp->done, 0);
     if (e != cudaSuccess) return cuda_fail(e, "stream wait");
     return MHA_OK;
 }
