@@ -14,6 +14,7 @@
 #include <string>
 
 #include "../../include/mha.h"
+#include "gemm_pair.h"
 #include "mha_internal.h"
 
 namespace {
@@ -92,12 +93,41 @@ mha_status_t map_rows(CUtensorMap* m, const void* base, int B, int L, int N, con
     const uint32_t box[3] = {64, 128, 1};
     return encode_bf16(m, base, 3, dims, str, box, what);
 }
-// weight [N, K] as {K, N}, box {64, kGemmBN}
-mha_status_t map_weight(CUtensorMap* m, const void* base, int N, int K) {
+// weight [N, K] as {K, N}, box {64, rows}: kGemmBN rows for the one-SM GEMM, half of
+// that for the pair GEMM (each CTA of a pair loads its half of the 256 columns)
+mha_status_t map_weight(CUtensorMap* m, const void* base, int N, int K, int rows) {
     const uint64_t dims[2] = {(uint64_t)K, (uint64_t)N};
     const uint64_t str[1] = {(uint64_t)K * 2};
-    const uint32_t box[2] = {64, (uint32_t)mha::kGemmBN};
+    const uint32_t box[2] = {64, (uint32_t)rows};
     return encode_bf16(m, base, 2, dims, str, box, "weight");
+}
+
+// Launch a projection GEMM whose groups, input and output maps are set: the pair
+// kernel (two SMs per 256-row tile, one MMA of M = 256) when every group has at
+// least 512 rows per batch item and there is at least a full wave of SM pairs,
+// else the one-SM kernel. Builds the weight maps W[g] ([N, K]) for the chosen one.
+mha_status_t launch_projection(mha::GemmParams& p, const void* const* W, cudaStream_t s, const char* what) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess)
+        return fail(MHA_ERR_CUDA, "device query failed");
+    const int n_tiles = (p.N + mha::kGemmBN - 1) / mha::kGemmBN;
+    bool pair = true;
+    long units = 0;
+    int max_m = 0;
+    for (int g = 0; g < p.ngroups; ++g) {
+        if (p.g[g].L < 4 * mha::kGemmBM) pair = false;
+        units += static_cast<long>(p.g[g].m_tiles / p.g[g].tiles_per_b) *
+                 ((p.g[g].L + 2 * mha::kGemmBM - 1) / (2 * mha::kGemmBM)) * n_tiles;
+        max_m = std::max(max_m, p.g[g].m_tiles);
+    }
+    if (units < sms / 2) pair = false;
+    mha_status_t st;
+    for (int g = 0; g < p.ngroups; ++g)
+        if ((st = map_weight(&p.w[g], W[g], p.N, p.K, pair ? mha::kGemmBN / 2 : mha::kGemmBN)) != MHA_OK) return st;
+    cudaError_t e = pair ? mha::launch_gemm_tc2(p, s) : mha::launch_gemm_tc(p, max_m, s);
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    return MHA_OK;
 }
 // head-split [B, planes, L_stride, d_k] (first L rows of each plane used), d_k = 64 * dks, as
 // {64, dks, L, planes, B}: a 64-column slab is (0, half, row, plane, b); box {64, 1, 128, 1, 1}
@@ -291,7 +321,6 @@ mha_status_t qkv_bf16_impl(const void* query, const void* key, const void* value
         if ((st = map_rows(&p.a[g], static_cast<const uint8_t*>(A[g]) + in_off, B, Ls[g], d_model,
                            "projection input", Lfull[g])) != MHA_OK)
             return st;
-        if ((st = map_weight(&p.w[g], W[g], d_model, d_model)) != MHA_OK) return st;
         if (g == 0) {
             if ((st = map_heads5(&p.out[g], ws + L.q + out_off, B, h, Ls[g], dk / 64, L_q)) != MHA_OK) return st;
         } else {
@@ -312,9 +341,8 @@ mha_status_t qkv_bf16_impl(const void* query, const void* key, const void* value
     p.dk_slabs = dk / 64;
     p.status = device_status_ptr();
     if (!p.status) return fail(MHA_ERR_CUDA, "device status word unavailable");
-    cudaError_t e = mha::launch_gemm_tc(p, max_m, s);
-    if (e != cudaSuccess) return cuda_fail(e, "QKV projection launch");
-    return MHA_OK;
+    (void)max_m;
+    return launch_projection(p, W, s, "QKV projection launch");
 }
 
 }  // namespace
@@ -421,7 +449,6 @@ mha_status_t output_projection_impl(mha_dtype_t dt, const void* w_o, const void*
     const int Lw = rows > 0 ? rows : L_q;
     const size_t off = static_cast<size_t>(r0) * d_model * 2;
     if ((st = map_rows(&p.a[0], ws + L.ctx + off, B, Lw, d_model, "context", L_q)) != MHA_OK) return st;
-    if ((st = map_weight(&p.w[0], w_o, d_model, d_model)) != MHA_OK) return st;
     if ((st = map_rows(&p.out[0], static_cast<uint8_t*>(out) + off, B, Lw, d_model, "output", L_q)) != MHA_OK)
         return st;
     if (residual && rows > 0)   // the epilogue indexes the residual with the window's own row count
@@ -437,9 +464,8 @@ mha_status_t output_projection_impl(mha_dtype_t dt, const void* w_o, const void*
     p.out_plain = 1;
     p.status = device_status_ptr();
     if (!p.status) return fail(MHA_ERR_CUDA, "device status word unavailable");
-    cudaError_t e = mha::launch_gemm_tc(p, p.g[0].m_tiles, s);
-    if (e != cudaSuccess) return cuda_fail(e, "output projection launch");
-    return MHA_OK;
+    const void* W[1] = {w_o};
+    return launch_projection(p, W, s, "output projection launch");
 }
 
 }  // namespace
@@ -581,7 +607,6 @@ mha_status_t mha_kv_cache_prefill(mha_dtype_t dt, const void* x, const void* w_k
     void* cache[2] = {k_cache, v_cache};
     for (int g = 0; g < 2; ++g) {
         if ((st = map_rows(&p.a[g], x, B, T, d_model, "prefill input")) != MHA_OK) return st;
-        if ((st = map_weight(&p.w[g], W[g], d_model, d_model)) != MHA_OK) return st;
         if ((st = map_heads5(&p.out[g], cache[g], B, h, T, 1, L_max)) != MHA_OK) return st;
         p.g[g].L = T;
         p.g[g].tiles_per_b = (T + mha::kGemmBM - 1) / mha::kGemmBM;
@@ -595,9 +620,7 @@ mha_status_t mha_kv_cache_prefill(mha_dtype_t dt, const void* x, const void* w_k
     p.dk_slabs = 1;
     p.status = device_status_ptr();
     if (!p.status) return fail(MHA_ERR_CUDA, "device status word unavailable");
-    cudaError_t e = mha::launch_gemm_tc(p, p.g[0].m_tiles, as_stream(stream));
-    if (e != cudaSuccess) return cuda_fail(e, "cache prefill launch");
-    return MHA_OK;
+    return launch_projection(p, W, as_stream(stream), "cache prefill launch");
 }
 
 mha_status_t mha_decode_step(mha_dtype_t dt, const void* x_new, const void* w_q, const void* b_q, const void* w_k,
@@ -714,7 +737,6 @@ mha_status_t mha_ffn_forward(mha_dtype_t dt, const void* x, const void* w_1, con
         const void* A = layer == 0 ? x : workspace;
         void* O = layer == 0 ? workspace : out;
         if ((st = map_rows(&p.a[0], A, B, L, K, "FFN input")) != MHA_OK) return st;
-        if ((st = map_weight(&p.w[0], layer == 0 ? w_1 : w_2, N, K)) != MHA_OK) return st;
         if ((st = map_rows(&p.out[0], O, B, L, N, "FFN output")) != MHA_OK) return st;
         p.g[0].L = L;
         p.g[0].tiles_per_b = tiles_per_b;
@@ -726,8 +748,9 @@ mha_status_t mha_ffn_forward(mha_dtype_t dt, const void* x, const void* w_1, con
         p.out_plain = 1;
         p.relu = layer == 0;
         p.status = status;
-        cudaError_t e = mha::launch_gemm_tc(p, p.g[0].m_tiles, s);
-        if (e != cudaSuccess) return cuda_fail(e, layer == 0 ? "FFN layer 1 launch" : "FFN layer 2 launch");
+        const void* W[1] = {layer == 0 ? w_1 : w_2};
+        if ((st = launch_projection(p, W, s, layer == 0 ? "FFN layer 1 launch" : "FFN layer 2 launch")) != MHA_OK)
+            return st;
     }
     return MHA_OK;
 }
