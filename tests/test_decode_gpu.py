@@ -119,3 +119,20 @@ def test_full_cache_is_reported_not_written(bnd):
     assert c.len.cpu().tolist() == [8, 8]
     assert torch.equal(c.k, k_before)
     assert bnd.mha_check_device_status(reset=True) == 0x301
+
+
+@pytest.mark.parametrize("B", [17, 40, 64, 70])
+def test_decode_batch_sizes(bnd, B):
+    """Projections of the step: up to 64 new tokens stream W over many CTAs in passes of
+    16 rows (17, 40: a partial last pass); 70 tokens use the tiled projection GEMM."""
+    T0, d, h = 100, 512, 8
+    inp = W.random_case(410 + B, B, T0 + 1, T0 + 1, d, h, self_attn=True, bias_scale=0.1)
+    c = Cache(bnd, inp, L_max=128)
+    c.prefill(inp.query[:, :T0])
+    got = c.step(inp.query[:, T0])
+    torch.cuda.synchronize()
+    w = [inp.weights[n] for n in WN]
+    ref = oracle.mha_forward(inp.query, inp.query, inp.query, *w, h, causal=True, rows=[T0])
+    _check(got.double().cpu().numpy(), ref[:, 0])
+    assert c.len.cpu().tolist() == [T0 + 1] * B
+    assert bnd.mha_check_device_status(reset=True) == 0

@@ -13,11 +13,13 @@
 //   kv_append_kernel    copies the new token's projected k, v (head-split) into
 //                       the caches at position cache_len[b] and increments it.
 //   decode_attn_kernel  split-K over the cached keys: each CTA takes a chunk of
-//                       keys of one (batch, head); a warp scores 32 keys at a
-//                       time (one key row per lane, 128-byte loads), keeps an
-//                       online softmax (running max and sum) and accumulates
-//                       p.V with two output features per lane; the CTA's warps
-//                       merge and write a partial (max, sum, o[64]).
+//                       keys of one (batch, head); a warp takes 32 keys at a
+//                       time with coalesced loads (each instruction reads 4
+//                       whole key or value rows), scores them with partial dot
+//                       products and an 8-lane reduce-scatter, keeps an online
+//                       softmax (running max and sum) and accumulates p.V per
+//                       lane over its own keys; the CTA's warps merge and write
+//                       a partial (max, sum, o[64]).
 //   decode_combine_kernel  merges the partials of a (batch, head) and writes
 //                       its 64-wide slab of the concatenated context.
 #include <math_constants.h>
@@ -76,72 +78,104 @@ __global__ void __launch_bounds__(32 * kWarps) decode_attn_kernel(const DecodePa
     const int chunk = ((n + p.n_split - 1) / p.n_split + 31) & ~31;
     const int c0 = blockIdx.x * chunk;
     const int c1 = min(n, c0 + chunk);
+    // Lane (grp, sl) = (lane / 8, lane % 8) holds dims 8 sl .. 8 sl + 7 of the keys
+    // 4 i + grp (i = 0..7) of each group of 32: every load instruction of the warp
+    // reads 4 whole consecutive key (or value) rows, 512 contiguous bytes.
+    const int grp = lane >> 3;
+    const int sl = lane & 7;
 
-    // the query row of (b, head), fp32 in registers (same for every lane)
-    const __nv_bfloat16* qp = p.q_new + (static_cast<long>(head) * p.B + b) * kD;
-    float q[kD];
-#pragma unroll
-    for (int c = 0; c < kD; c += 8) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(qp + c);
+    // this lane's slice of the query row, pre-scaled so that scores are in log2 units
+    float q[8];
+    {
+        const uint4 raw = *reinterpret_cast<const uint4*>(p.q_new + (static_cast<long>(head) * p.B + b) * kD + 8 * sl);
         const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const float2 f = __bfloat1622float2(h2[e]);
-            q[c + 2 * e] = f.x * p.scale_log2;   // scores in log2 units
-            q[c + 2 * e + 1] = f.y * p.scale_log2;
+            q[2 * e] = f.x * p.scale_log2;
+            q[2 * e + 1] = f.y * p.scale_log2;
         }
     }
-    const __nv_bfloat16* K = p.k_cache + static_cast<long>(bh) * p.L_max * kD;
-    const __nv_bfloat16* V = p.v_cache + static_cast<long>(bh) * p.L_max * kD;
-    float m = -CUDART_INF_F, l = 0.0f, o0 = 0.0f, o1 = 0.0f;
-    for (int g = c0 + 32 * warp; g < c1; g += 32 * kWarps) {
-        const int key = g + lane;
-        const int cnt = c1 - g;
-        // issue this group's key row (one per lane) and value rows (one 128-byte row per key,
-        // two features per lane) together, so both memory latencies overlap
-        uint4 kraw[kD / 8];
+    const __nv_bfloat16* K = p.k_cache + static_cast<long>(bh) * p.L_max * kD + 8 * sl;
+    const __nv_bfloat16* V = p.v_cache + static_cast<long>(bh) * p.L_max * kD + 8 * sl;
+    float m = -CUDART_INF_F, l = 0.0f;
+    float o[8];   // partial p.V over this lane's keys, dims 8 sl ..
 #pragma unroll
-        for (int c = 0; c < kD / 8; ++c)
-            kraw[c] = (key < c1) ? *reinterpret_cast<const uint4*>(K + static_cast<long>(key) * kD + 8 * c)
-                                 : make_uint4(0, 0, 0, 0);
-        __nv_bfloat162 vr[32];
+    for (int f = 0; f < 8; ++f) o[f] = 0.0f;
+    for (int g0 = c0 + 32 * warp; g0 < c1; g0 += 32 * kWarps) {
+        // keys and values of the group, all 16 loads in flight together
+        uint4 kr[8], vr[8];
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-            vr[j] = (j < cnt) ? *reinterpret_cast<const __nv_bfloat162*>(V + static_cast<long>(g + j) * kD + 2 * lane)
-                              : __floats2bfloat162_rn(0.0f, 0.0f);
-        float acc = 0.0f;
+        for (int i = 0; i < 8; ++i) {
+            const int key = g0 + 4 * i + grp;
+            kr[i] = (key < c1) ? *reinterpret_cast<const uint4*>(K + static_cast<long>(key) * kD) : make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
-        for (int c = 0; c < kD / 8; ++c) {
-            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&kraw[c]);
+        for (int i = 0; i < 8; ++i) {
+            const int key = g0 + 4 * i + grp;
+            vr[i] = (key < c1) ? *reinterpret_cast<const uint4*>(V + static_cast<long>(key) * kD) : make_uint4(0, 0, 0, 0);
+        }
+        // partial scores of the 8 keys over this lane's 8 dims
+        float part[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&kr[i]);
+            float a = 0.0f;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const float2 f = __bfloat1622float2(h2[e]);
-                acc = fmaf(q[8 * c + 2 * e], f.x, acc);
-                acc = fmaf(q[8 * c + 2 * e + 1], f.y, acc);
+                a = fmaf(q[2 * e], f.x, a);
+                a = fmaf(q[2 * e + 1], f.y, a);
+            }
+            part[i] = a;
+        }
+        // reduce-scatter over the 8 lanes of the group: lane sl ends with the whole score
+        // of its key i = sl, i.e. key g0 + 4 sl + grp
+#pragma unroll
+        for (int s = 4; s >= 1; s >>= 1) {
+            const bool upper = (sl & s) != 0;
+#pragma unroll
+            for (int t = 0; t < s; ++t) {
+                const float send = upper ? part[t] : part[t + s];
+                const float keep = upper ? part[t + s] : part[t];
+                part[t] = keep + __shfl_xor_sync(0xffffffffu, send, s);
             }
         }
-        const float s = (key < c1) ? acc : -CUDART_INF_F;
-        const float m_new = fmaxf(m, warp_max(s));   // finite: key g < c1 always exists
+        const float sc = (g0 + 4 * sl + grp < c1) ? part[0] : -CUDART_INF_F;
+        const float m_new = fmaxf(m, warp_max(sc));   // finite: key g0 < c1 always exists
         const float alpha = ex2_approx(m - m_new);
-        const float pj = ex2_approx(s - m_new);      // 0 for keys past the chunk
+        const float pj = ex2_approx(sc - m_new);      // 0 for keys past the chunk
         l = l * alpha + warp_sum(pj);
-        o0 *= alpha;
-        o1 *= alpha;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const float w = __shfl_sync(0xffffffffu, pj, j);
-            const float2 v = __bfloat1622float2(vr[j]);
-            o0 = fmaf(w, v.x, o0);
-            o1 = fmaf(w, v.y, o1);
+        for (int f = 0; f < 8; ++f) o[f] *= alpha;
+        // this lane's value rows are keys 4 i + grp, whose weights sit in lanes 8 grp + i
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float w = __shfl_sync(0xffffffffu, pj, 8 * grp + i);
+            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&vr[i]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 v = __bfloat1622float2(h2[e]);
+                o[2 * e] = fmaf(w, v.x, o[2 * e]);
+                o[2 * e + 1] = fmaf(w, v.y, o[2 * e + 1]);
+            }
         }
         m = m_new;
+    }
+    // lanes with the same dims (sl) hold partials over disjoint keys: sum the 4 groups
+#pragma unroll
+    for (int f = 0; f < 8; ++f) {
+        o[f] += __shfl_xor_sync(0xffffffffu, o[f], 8);
+        o[f] += __shfl_xor_sync(0xffffffffu, o[f], 16);
     }
     if (lane == 0) {
         sm_m[warp] = m;
         sm_l[warp] = l;
     }
-    sm_o[warp][2 * lane] = o0;
-    sm_o[warp][2 * lane + 1] = o1;
+    if (lane < 8) {
+#pragma unroll
+        for (int f = 0; f < 8; ++f) sm_o[warp][8 * lane + f] = o[f];
+    }
     __syncthreads();
     if (warp == 0) {
         float M = -CUDART_INF_F;

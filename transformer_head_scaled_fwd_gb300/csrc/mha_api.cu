@@ -15,6 +15,7 @@
 
 #include "../../include/mha.h"
 #include "gemm_pair.h"
+#include "gemv.h"
 #include "mha_internal.h"
 
 namespace {
@@ -643,13 +644,30 @@ mha_status_t mha_decode_step(mha_dtype_t dt, const void* x_new, const void* w_q,
         if (ptr && !aligned16(ptr)) return fail(MHA_ERR_INVALID_ARG, "bf16 tensors must be 16-byte aligned");
     if (!aligned16(out)) return fail(MHA_ERR_INVALID_ARG, "bf16 tensors must be 16-byte aligned");
     const size_t ws_mha = mha_workspace_size(MHA_BF16, 1, B, B, d_model, h);
-    // 1. q, k, v of the B new tokens: the projection GEMM on a [1, B, d_model] view
-    if ((st = mha_qkv_projection(dt, x_new, x_new, x_new, w_q, b_q, w_k, b_k, w_v, b_v, 1, B, B, d_model, h,
-                                 workspace, ws_mha, stream)) != MHA_OK)
-        return st;
     Layout L;
     layout_of(dt, 1, B, B, d_model, h, &L);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const bool gemv = mha::gemv_supported(B, d_model);   // a few rows: stream W over many CTAs
+    // 1. q, k, v of the B new tokens, head-split as for a [1, B, d_model] sequence
+    if (gemv) {
+        mha::GemvParams g{};
+        g.x = static_cast<const __nv_bfloat16*>(x_new);
+        const void* W[3] = {w_q, w_k, w_v};
+        const void* bias[3] = {b_q, b_k, b_v};
+        for (int i = 0; i < 3; ++i) {
+            g.w[i] = static_cast<const __nv_bfloat16*>(W[i]);
+            g.bias[i] = static_cast<const __nv_bfloat16*>(bias[i]);
+        }
+        g.out[0] = reinterpret_cast<__nv_bfloat16*>(ws + L.q);
+        g.out[1] = g.out[2] = reinterpret_cast<__nv_bfloat16*>(ws + L.kv);
+        g.j0[0] = 0; g.j0[1] = 0; g.j0[2] = h;
+        g.M = B; g.N = d_model; g.K = d_model; g.ngroups = 3; g.head_split = 1;
+        cudaError_t e = mha::launch_gemv_bf16(g, as_stream(stream));
+        if (e != cudaSuccess) return cuda_fail(e, "decode Q/K/V projection launch");
+    } else if ((st = mha_qkv_projection(dt, x_new, x_new, x_new, w_q, b_q, w_k, b_k, w_v, b_v, 1, B, B, d_model, h,
+                                        workspace, ws_mha, stream)) != MHA_OK) {
+        return st;
+    }
     mha::DecodeParams p{};
     p.q_new = reinterpret_cast<const __nv_bfloat16*>(ws + L.q);
     p.kv_new = reinterpret_cast<const __nv_bfloat16*>(ws + L.kv);
@@ -672,6 +690,17 @@ mha_status_t mha_decode_step(mha_dtype_t dt, const void* x_new, const void* w_q,
     e = mha::launch_decode_attention(p, s);
     if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
     // 5. out = ctx W_o^T + b_o
+    if (gemv) {
+        mha::GemvParams g{};
+        g.x = reinterpret_cast<const __nv_bfloat16*>(ws + L.ctx);
+        g.w[0] = static_cast<const __nv_bfloat16*>(w_o);
+        g.bias[0] = static_cast<const __nv_bfloat16*>(b_o);
+        g.out[0] = static_cast<__nv_bfloat16*>(out);
+        g.M = B; g.N = d_model; g.K = d_model; g.ngroups = 1; g.head_split = 0;
+        e = mha::launch_gemv_bf16(g, s);
+        if (e != cudaSuccess) return cuda_fail(e, "decode output projection launch");
+        return MHA_OK;
+    }
     return output_projection_impl(dt, w_o, b_o, nullptr, 1, B, d_model, h, out, L, ws, s);
 }
 
