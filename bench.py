@@ -596,7 +596,7 @@ def run_gpu_decode(args):
     peaks, peak_src = load_peaks()
     Bn, d, h, P = args.decode_batch, 1024, 16, args.decode_context
     K, Wm = args.steps, args.warmup
-    L_max = P + K + Wm + 8
+    L_max = P + 2 * (K + Wm) + 8   # room for the direct loop and the graph replays
     inp = W.random_case(500 + rank, Bn, P + 1, P + 1, d, h, self_attn=True, bias_scale=0.0)
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda().to(torch.bfloat16)
     w = [dev(inp.weights[n]) for n in ("w_q", "b_q", "w_k", "b_k", "w_v", "b_v", "w_o", "b_o")]
@@ -619,9 +619,23 @@ def run_gpu_decode(args):
                                     stream=stream)
             evs[s_][1].record(stream)
         torch.cuda.synchronize()
+        # the same step captured once in a CUDA graph and replayed (cache_len lives on the
+        # device, so every replay appends the next token); L2 flushed between replays
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            binding.mha_decode_step(x_new, *w, h, k_cache=kc, v_cache=vc, cache_len=clen, out=out, workspace=ws,
+                                    stream=torch.cuda.current_stream())
+        g_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K + Wm)]
+        for s_ in range(Wm + K):
+            flush.zero_()
+            g_evs[s_][0].record(stream)
+            graph.replay()
+            g_evs[s_][1].record(stream)
+        torch.cuda.synchronize()
     if binding.mha_check_device_status(reset=True) != 0:
         raise RuntimeError("a kernel reported an error")
     ms = sum(a.elapsed_time(b) for a, b in evs[Wm:]) / K
+    g_ms = sum(a.elapsed_time(b) for a, b in g_evs[Wm:]) / K
     mean_ctx = P + Wm + (K + 1) / 2.0          # cached tokens attended per step, on average
     cache_bytes = Bn * h * mean_ctx * 64 * 2 * 2
     bytes_step = cache_bytes + 4 * d * d * 2 + 4 * Bn * d * 2 + Bn * h * 64 * 2 * 2
@@ -636,6 +650,8 @@ def run_gpu_decode(args):
         "roofline": {"kernel": "decode step (projection GEMMs + split-K cache attention)", "bound": "hbm",
                      "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak, "traffic": None,
                      "algorithmic_bytes_per_step": bytes_step, "peak_source": f"{peak_src} hbm_gbs"},
+        "graph": {"ms_per_step": g_ms, "value": Bn / (g_ms * 1e-3), "unit": "tokens/s",
+                  "note": "the step captured once in a CUDA graph, replayed; L2 flushed between replays"},
         "gpu_launches": 8 * K, "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)

@@ -10,8 +10,10 @@
 // cached keys, no mask needed (every cached position precedes the query).
 //
 // Kernels (HBM-bound: the cache is read once per step):
-//   kv_append_kernel    copies the new token's projected k, v (head-split) into
-//                       the caches at position cache_len[b] and increments it.
+//   kv_append_kernel    (steps with more than 64 new tokens, whose projections
+//                       run as tiled GEMMs) copies the new token's projected k, v
+//                       into the caches at position cache_len[b]; with fewer, the
+//                       projection kernel writes them there itself.
 //   decode_attn_kernel  split-K over the cached keys: each CTA takes a chunk of
 //                       keys of one (batch, head); a warp takes 32 keys at a
 //                       time with coalesced loads (each instruction reads 4
@@ -20,8 +22,9 @@
 //                       softmax (running max and sum) and accumulates p.V per
 //                       lane over its own keys; the CTA's warps merge and write
 //                       a partial (max, sum, o[64]).
-//   decode_combine_kernel  merges the partials of a (batch, head) and writes
-//                       its 64-wide slab of the concatenated context.
+//   decode_combine_kernel  merges the partials of a (batch, head), writes its
+//                       64-wide slab of the concatenated context, and counts the
+//                       new token in cache_len[b] (or reports a full cache).
 #include <math_constants.h>
 
 #include "mha_internal.h"
@@ -36,11 +39,7 @@ constexpr int kWarps = 4;
 __global__ void __launch_bounds__(256) kv_append_kernel(const DecodeParams p) {
     const int b = blockIdx.x;
     const int pos = p.cache_len[b];
-    __syncthreads();   // every thread has read the old length before it is incremented
-    if (pos < 0 || pos >= p.L_max) {
-        if (threadIdx.x == 0) atomicCAS(p.status, 0, 0x301);   // cache full: nothing appended
-        return;
-    }
+    if (pos < 0 || pos >= p.L_max) return;   // full cache: nothing appended (reported by the combine)
     // KVh of the step is [1, 2, h, B, 64]: k of (b, head) at ((head) * B + b) * 64, v after h planes
     for (int e = threadIdx.x; e < p.h * kD / 8; e += blockDim.x) {
         const int head = e / (kD / 8);
@@ -51,8 +50,6 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const DecodeParams p) {
         *reinterpret_cast<uint4*>(p.k_cache + dst) = *reinterpret_cast<const uint4*>(p.kv_new + src);
         *reinterpret_cast<uint4*>(p.v_cache + dst) = *reinterpret_cast<const uint4*>(p.kv_new + vsrc);
     }
-    __syncthreads();
-    if (threadIdx.x == 0) p.cache_len[b] = pos + 1;
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -74,7 +71,8 @@ __global__ void __launch_bounds__(32 * kWarps) decode_attn_kernel(const DecodePa
     const int head = bh - b * p.h;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int n = min(max(p.cache_len[b], 0), p.L_max);
+    // the step's key and value sit at position cache_len[b] (unless the cache is full)
+    const int n = min(max(p.cache_len[b], 0) + 1, p.L_max);
     const int chunk = ((n + p.n_split - 1) / p.n_split + 31) & ~31;
     const int c0 = blockIdx.x * chunk;
     const int c1 = min(n, c0 + chunk);
@@ -205,18 +203,36 @@ __global__ void __launch_bounds__(kD) decode_combine_kernel(const DecodeParams p
     const int head = bh - b * p.h;
     const int c = threadIdx.x;
     const float* part = p.partial + static_cast<long>(bh) * p.n_split * (kD + 2);
+    // all partials of this thread's column in flight together (n_split <= kDecodeMaxSplit)
+    float ms[kDecodeMaxSplit], ls[kDecodeMaxSplit], os[kDecodeMaxSplit];
     float M = -CUDART_INF_F;
-    for (int s = 0; s < p.n_split; ++s) M = fmaxf(M, part[s * (kD + 2)]);
+#pragma unroll
+    for (int s = 0; s < kDecodeMaxSplit; ++s) {
+        if (s < p.n_split) {
+            ms[s] = part[s * (kD + 2)];
+            ls[s] = part[s * (kD + 2) + 1];
+            os[s] = part[s * (kD + 2) + 2 + c];
+            M = fmaxf(M, ms[s]);
+        }
+    }
     float L = 0.0f, acc = 0.0f;
-    for (int s = 0; s < p.n_split; ++s) {
-        const float ms = part[s * (kD + 2)];
-        if (ms == -CUDART_INF_F) continue;   // empty chunk
-        const float f = ex2_approx(ms - M);
-        L += part[s * (kD + 2) + 1] * f;
-        acc += part[s * (kD + 2) + 2 + c] * f;
+#pragma unroll
+    for (int s = 0; s < kDecodeMaxSplit; ++s) {
+        if (s < p.n_split && ms[s] != -CUDART_INF_F) {   // skip empty chunks
+            const float f = ex2_approx(ms[s] - M);
+            L += ls[s] * f;
+            acc += os[s] * f;
+        }
     }
     // ctx of the step is [1, B, d_model]: the head's slab of row b
     p.ctx[static_cast<long>(b) * p.h * kD + head * kD + c] = __float2bfloat16_rn(acc / L);
+    if (head == 0 && c == 0) {   // every read of the old length is done: count the new token
+        const int len = p.cache_len[b];
+        if (len >= 0 && len < p.L_max)
+            p.cache_len[b] = len + 1;
+        else
+            atomicCAS(p.status, 0, 0x301);   // cache full: the token was not appended
+    }
 }
 
 }  // namespace

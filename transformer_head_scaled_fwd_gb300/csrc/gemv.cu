@@ -8,8 +8,9 @@
 // rows staged in shared memory (16 rows per pass), accumulating 2 x 16 sums in
 // fp32. A 5-step butterfly (reduce-scatter over the 32 lanes) leaves lane l with
 // the complete sum of (feature l / 16, row l % 16), which it finishes with the
-// bias and stores as bf16: head-split [planes, M, 64] (the q / k / v of the
-// step) or plain [M, N].
+// bias and stores as bf16: head-split [planes, M, 64] (the q of the step),
+// straight into the key / value caches at each sequence's current length (k and v
+// of the step), or plain [M, N].
 #include "gemv.h"
 
 namespace mha {
@@ -52,10 +53,19 @@ __global__ void __launch_bounds__(32 * kGemvWarps) gemv_bf16_kernel(const __grid
 
     for (int mb = 0; mb < p.M; mb += kGemvRows) {
         __syncthreads();   // the previous pass has finished reading xs
-        for (int i = threadIdx.x; i < kGemvRows * K / 8; i += blockDim.x) {
-            const int r = i / (K / 8), c = i - r * (K / 8);
-            xs[i] = (mb + r < p.M) ? *reinterpret_cast<const uint4*>(p.x + static_cast<long>(mb + r) * K + c * 8)
-                                   : make_uint4(0, 0, 0, 0);
+        {
+            // every thread's 16-byte loads of the 16 x rows in flight together
+            constexpr int kPer = kGemvRows * KC * 32 / (32 * kGemvWarps);
+            uint4 t[kPer];
+#pragma unroll
+            for (int u = 0; u < kPer; ++u) {
+                const int i = threadIdx.x + u * 32 * kGemvWarps;
+                const int r = i / (K / 8), c = i - r * (K / 8);
+                t[u] = (mb + r < p.M) ? *reinterpret_cast<const uint4*>(p.x + static_cast<long>(mb + r) * K + c * 8)
+                                      : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < kPer; ++u) xs[threadIdx.x + u * 32 * kGemvWarps] = t[u];
         }
         __syncthreads();
         float acc[2 * kGemvRows];   // index f * 16 + row
@@ -94,12 +104,19 @@ __global__ void __launch_bounds__(32 * kGemvWarps) gemv_bf16_kernel(const __grid
         if (n < p.N && m < p.M) {
             float y = acc[0];
             if (p.bias[g]) y += __bfloat162float(p.bias[g][n]);
-            long off;
-            if (p.head_split)   // plane j0 + n / 64, row m, column n % 64 of [planes, M, 64]
-                off = (static_cast<long>(p.j0[g] + n / 64) * p.M + m) * 64 + (n & 63);
-            else
-                off = static_cast<long>(m) * p.N + n;
-            p.out[g][off] = __float2bfloat16_rn(y);
+            if (g > 0 && p.k_cache != nullptr) {   // the step's key / value: straight into the cache
+                const int pos = p.cache_len[m];
+                if (pos >= 0 && pos < p.L_max)
+                    (g == 1 ? p.k_cache : p.v_cache)[((static_cast<long>(m) * (p.N / 64) + n / 64) * p.L_max + pos) *
+                                                          64 + (n & 63)] = __float2bfloat16_rn(y);
+            } else {
+                long off;
+                if (p.head_split)   // plane j0 + n / 64, row m, column n % 64 of [planes, M, 64]
+                    off = (static_cast<long>(p.j0[g] + n / 64) * p.M + m) * 64 + (n & 63);
+                else
+                    off = static_cast<long>(m) * p.N + n;
+                p.out[g][off] = __float2bfloat16_rn(y);
+            }
         }
     }
 }

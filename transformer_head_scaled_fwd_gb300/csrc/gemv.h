@@ -17,6 +17,14 @@ struct GemvParams {
     int j0[3];                       // head-split: first plane of this matrix's output
     int M, N, K, ngroups;
     int head_split;
+    // Key/value caches (decode): when k_cache != nullptr, matrices 1 and 2 write row m
+    // (sequence m) into k_cache / v_cache [M, N / 64, L_max, 64] at position
+    // cache_len[m] instead of out[1] / out[2]; nothing is written when that position
+    // is not below L_max (full cache).
+    __nv_bfloat16* k_cache;
+    __nv_bfloat16* v_cache;
+    const int32_t* cache_len;
+    int L_max;
 };
 
 bool gemv_supported(int M, int K);   // K in {256, 512, 1024, 2048}, 1 <= M <= kGemvMaxRows

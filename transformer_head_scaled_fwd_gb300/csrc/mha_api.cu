@@ -662,6 +662,10 @@ mha_status_t mha_decode_step(mha_dtype_t dt, const void* x_new, const void* w_q,
         g.out[1] = g.out[2] = reinterpret_cast<__nv_bfloat16*>(ws + L.kv);
         g.j0[0] = 0; g.j0[1] = 0; g.j0[2] = h;
         g.M = B; g.N = d_model; g.K = d_model; g.ngroups = 3; g.head_split = 1;
+        g.k_cache = static_cast<__nv_bfloat16*>(k_cache);   // k, v of the step go straight to the caches
+        g.v_cache = static_cast<__nv_bfloat16*>(v_cache);
+        g.cache_len = cache_len;
+        g.L_max = L_max;
         cudaError_t e = mha::launch_gemv_bf16(g, as_stream(stream));
         if (e != cudaSuccess) return cuda_fail(e, "decode Q/K/V projection launch");
     } else if ((st = mha_qkv_projection(dt, x_new, x_new, x_new, w_q, b_q, w_k, b_k, w_v, b_v, 1, B, B, d_model, h,
@@ -684,9 +688,10 @@ mha_status_t mha_decode_step(mha_dtype_t dt, const void* x_new, const void* w_q,
     p.status = device_status_ptr();
     if (!p.status) return fail(MHA_ERR_CUDA, "device status word unavailable");
     const cudaStream_t s = as_stream(stream);
-    // 2. append k, v at cache_len[b] (incremented); 3. attention over the cache; 4. merge
-    cudaError_t e = mha::launch_kv_append(p, s);
-    if (e != cudaSuccess) return cuda_fail(e, "cache append launch");
+    // 2. (tiled projections only) append k, v at cache_len[b]; 3. attention over the cache,
+    // the new token included; 4. merge, and count the new token in cache_len[b]
+    cudaError_t e = cudaSuccess;
+    if (!gemv && (e = mha::launch_kv_append(p, s)) != cudaSuccess) return cuda_fail(e, "cache append launch");
     e = mha::launch_decode_attention(p, s);
     if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
     // 5. out = ctx W_o^T + b_o

@@ -130,10 +130,10 @@ cudaError_t launch_attn_f32(const F32AttnParams& p, cudaStream_t s);
 // ------------------------------------------------------------ incremental decoding (d_k = 64, bf16)
 struct DecodeParams {
     const __nv_bfloat16* q_new;    // Qh of the step [1, h, B, 64]
-    const __nv_bfloat16* kv_new;   // KVh of the step [1, 2, h, B, 64]
+    const __nv_bfloat16* kv_new;   // KVh of the step [1, 2, h, B, 64] (tiled projections only)
     __nv_bfloat16* k_cache;        // [B, h, L_max, 64]
     __nv_bfloat16* v_cache;        // [B, h, L_max, 64]
-    int32_t* cache_len;            // [B], incremented by the append kernel
+    int32_t* cache_len;            // [B]; the step's token sits at cache_len[b], counted by the combine kernel
     __nv_bfloat16* ctx;            // [1, B, h * 64]
     float* partial;                // [B * h, n_split, 66]: max (log2 units), sum, o[64]
     int B, h, L_max, n_split;
