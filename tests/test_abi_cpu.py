@@ -50,6 +50,24 @@ def test_workspace_size_layout(lib):
     assert binding.workspace_size(binding.MHA_F32, 0, Lq, Lk, d, h) == 0
 
 
+def test_workspace_size_bf16_other_head_widths(lib):
+    """bf16 with d_k outside {64, 128} runs on the fp32 kernels over fp32 copies: the
+    workspace is the fp32 forward's, then query, key, value, 4 weights, 4 biases and out
+    in fp32, each part 256-aligned."""
+    B_, Lq, Lk, d, h = 2, 10, 7, 192, 2
+    a = lambda x: (x + 255) // 256 * 256
+    f32 = binding.workspace_size(binding.MHA_F32, B_, Lq, Lk, d, h)
+    qn, kn = 4 * B_ * Lq * d, 4 * B_ * Lk * d
+    off = a(f32)
+    off = a(off + qn)
+    off = a(off + kn)
+    off = a(off + kn)
+    off = a(off + 16 * d * d)
+    off = a(off + 16 * d)
+    assert binding.workspace_size(binding.MHA_BF16, B_, Lq, Lk, d, h) == a(off + qn)
+    assert binding.workspace_size(binding.MHA_BF16, B_, Lq, Lk, 640, 2) > 0    # sizes stay defined
+
+
 def _call_forward(lib, dt=binding.MHA_BF16, B_=1, Lq=4, Lk=4, d=128, h=2, mask=None, ws=1 << 30,
                   ws_ptr=256, ptr=4096):
     P = ctypes.c_void_p(ptr)
@@ -62,7 +80,7 @@ def test_validation_without_gpu(lib):
     assert _call_forward(lib, d=130, h=4) == binding.MHA_ERR_INVALID_ARG          # d % h != 0
     assert b"d_model % h" in lib.mha_last_error()
     assert _call_forward(lib, B_=0) == binding.MHA_ERR_INVALID_ARG
-    assert _call_forward(lib, d=192, h=2) == binding.MHA_ERR_UNSUPPORTED          # bf16 d_k = 96
+    assert _call_forward(lib, d=640, h=2) == binding.MHA_ERR_UNSUPPORTED          # d_k = 320 > 256
     assert _call_forward(lib, dt=binding.MHA_F32, d=1024, h=2) == binding.MHA_ERR_UNSUPPORTED
     assert _call_forward(lib, dt=7) == binding.MHA_ERR_INVALID_ARG
     m = binding.MaskT(); m.causal = 1

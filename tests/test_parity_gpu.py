@@ -225,11 +225,14 @@ def test_invalid_arguments_leave_output_untouched():
     with pytest.raises(binding.MHAError) as e:
         binding.mha_forward(x, x, x, w, None, w, None, w, None, w, None, 5, out=out, workspace=ws)
     assert e.value.status == binding.MHA_ERR_INVALID_ARG
-    with pytest.raises(binding.MHAError) as e:       # d_k = 48 on the bf16 path
-        binding.mha_forward(x, x, x, w, None, w, None, w, None, w, None, 2, out=out, workspace=ws)
+    x2 = torch.zeros(1, 8, 640, dtype=dt, device="cuda")
+    w2 = torch.zeros(640, 640, dtype=dt, device="cuda")
+    out2 = torch.full((1, 8, 640), 3.0, dtype=dt, device="cuda")
+    with pytest.raises(binding.MHAError) as e:       # d_k = 320: above the 256 the kernels take
+        binding.mha_forward(x2, x2, x2, w2, None, w2, None, w2, None, w2, None, 2, out=out2, workspace=ws)
     assert e.value.status == binding.MHA_ERR_UNSUPPORTED
     torch.cuda.synchronize()
-    assert torch.all(out == 3.0)
+    assert torch.all(out == 3.0) and torch.all(out2 == 3.0)
 
 
 def test_forward_host_uneven_chunks_distinct_kv_and_masks():
@@ -294,3 +297,17 @@ def test_forward_host_row_windows(h, masked):
     rows = [0, 1, 255, 256, 257, 511, 512, 639]
     ref = run_oracle(inp, rows=rows, **kw)
     assert_close(hout.double().numpy()[:, rows], ref, "bf16")
+
+
+@pytest.mark.parametrize("d,h", [(256, 8), (384, 4), (512, 2)])   # d_k 32, 96, 256
+def test_bf16_other_head_widths(d, h):
+    """bf16 problems whose head width the tensor-core kernels do not take run on the fp32
+    kernels over fp32 copies of the bf16 inputs: causal + key padding, p_attn."""
+    B, L = 2, 70
+    inp = W.random_case(130 + h, B, L, L, d, h, self_attn=True, bias_scale=0.1)
+    vl = [70, 33]
+    got, pa = run_gpu(inp, causal=True, valid_lens=vl, want_p_attn=True)
+    ref, ref_pa = run_oracle(inp, causal=True, valid_lens=vl, want_p_attn=True)
+    assert_close(got, ref, "bf16")
+    np.testing.assert_allclose(pa.sum(-1), 1.0, atol=1e-3)
+    assert np.abs(pa - ref_pa).max() < 5e-3

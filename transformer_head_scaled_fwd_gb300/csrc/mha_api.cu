@@ -16,6 +16,7 @@
 #include "../../include/mha.h"
 #include "gemm_pair.h"
 #include "gemv.h"
+#include "convert.h"
 #include "mha_internal.h"
 
 namespace {
@@ -45,6 +46,13 @@ struct Layout {
     size_t q, kv, ctx, stat, total;
 };
 
+// Workspace of a bf16 problem run on the fp32 kernels: the fp32 forward's own
+// workspace, then fp32 copies of query, key, value, the four weights and biases,
+// and the fp32 output.
+struct F32Copies {
+    size_t ws, q, k, v, w, b, out, total;
+};
+
 bool layout_of(mha_dtype_t dt, int B, int Lq, int Lk, int d, int h, Layout* L) {
     if (B <= 0 || Lq <= 0 || Lk <= 0 || d <= 0 || h <= 0 || d % h != 0) return false;
     if (dt != MHA_F32 && dt != MHA_BF16) return false;
@@ -56,6 +64,20 @@ bool layout_of(mha_dtype_t dt, int B, int Lq, int Lk, int d, int h, Layout* L) {
     L->stat = align256(L->ctx + es * B * static_cast<size_t>(Lq) * d);
     L->total = align256(L->stat + sizeof(float) * 2 * B * h * static_cast<size_t>(Lq));
     return true;
+}
+
+void f32_copies_of(int B, int Lq, int Lk, int d, int h, F32Copies* C) {
+    Layout L;
+    layout_of(MHA_F32, B, Lq, Lk, d, h, &L);
+    const size_t qn = 4ull * B * Lq * d, kn = 4ull * B * Lk * d;
+    C->ws = 0;
+    C->q = align256(L.total);
+    C->k = align256(C->q + qn);
+    C->v = align256(C->k + kn);
+    C->w = align256(C->v + kn);
+    C->b = align256(C->w + 4ull * 4 * d * d);
+    C->out = align256(C->b + 4ull * 4 * d);
+    C->total = align256(C->out + qn);
 }
 
 // ---------------------------------------------------------------- tensor maps
@@ -165,16 +187,20 @@ int* device_status_ptr() {
 // ---------------------------------------------------------------- validation
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-mha_status_t check_sizes(mha_dtype_t dt, int B, int Lq, int Lk, int d, int h) {
+// bf16 head widths the tensor-core kernels take; other widths up to 256 run (in
+// mha_forward only) on the fp32 kernels over converted copies.
+bool bf16_native_dk(int dk) { return dk == 64 || dk == 128; }
+
+mha_status_t check_sizes(mha_dtype_t dt, int B, int Lq, int Lk, int d, int h, bool bf16_any_dk = false) {
     if (dt != MHA_F32 && dt != MHA_BF16) return fail(MHA_ERR_INVALID_ARG, "dtype %d is not MHA_F32 or MHA_BF16", dt);
     if (B <= 0 || Lq <= 0 || Lk <= 0 || d <= 0 || h <= 0)
         return fail(MHA_ERR_INVALID_ARG, "sizes must be positive (B=%d L_q=%d L_k=%d d_model=%d h=%d)", B, Lq, Lk, d,
                     h);
     if (d % h != 0) return fail(MHA_ERR_INVALID_ARG, "d_model %% h != 0 (d_model=%d, h=%d)", d, h);
     const int dk = d / h;
-    if (dt == MHA_BF16 && dk != 64 && dk != 128)
-        return fail(MHA_ERR_UNSUPPORTED, "bf16 path implements d_k = 64 and 128 (d_k = %d)", dk);
-    if (dt == MHA_F32 && dk > 256) return fail(MHA_ERR_UNSUPPORTED, "fp32 path implements d_k <= 256 (d_k = %d)", dk);
+    if (dt == MHA_BF16 && !bf16_native_dk(dk) && !(bf16_any_dk && dk <= 256))
+        return fail(MHA_ERR_UNSUPPORTED, "this bf16 entry point implements d_k = 64 and 128 (d_k = %d)", dk);
+    if (dk > 256) return fail(MHA_ERR_UNSUPPORTED, "d_k <= 256 is implemented (d_k = %d)", dk);
     const double big = static_cast<double>(B) * h * Lq * Lk;
     if (static_cast<double>(B) * Lq * d > 4.0e9 || static_cast<double>(B) * Lk * d * 2 > 4.0e9 || big > 1.0e15)
         return fail(MHA_ERR_UNSUPPORTED, "problem too large for 32-bit tile indices");
@@ -215,6 +241,11 @@ mha_status_t attention_impl(mha_dtype_t dt, int B, int L_q, int L_k, int d_model
 mha_status_t output_projection_impl(mha_dtype_t dt, const void* w_o, const void* b_o, const void* residual,
                                     int B, int L_q, int d_model, int h, void* out, const Layout& L, uint8_t* ws,
                                     cudaStream_t s, int r0 = 0, int rows = 0);
+mha_status_t forward_bf16_on_f32(const void* query, const void* key, const void* value, const void* w_q,
+                                 const void* b_q, const void* w_k, const void* b_k, const void* w_v, const void* b_v,
+                                 const void* w_o, const void* b_o, int B, int L_q, int L_k, int d_model, int h,
+                                 const mha_mask_t* mask, void* out, float* p_attn, void* workspace,
+                                 size_t workspace_bytes, cudaStream_t s);
 
 }  // namespace
 
@@ -230,6 +261,11 @@ const char* mha_last_error(void) { return g_last_error.c_str(); }
 size_t mha_workspace_size(mha_dtype_t dt, int B, int L_q, int L_k, int d_model, int h) {
     Layout L;
     if (!layout_of(dt, B, L_q, L_k, d_model, h, &L)) return 0;
+    if (dt == MHA_BF16 && !bf16_native_dk(d_model / h) && d_model / h <= 256) {
+        F32Copies C;
+        f32_copies_of(B, L_q, L_k, d_model, h, &C);
+        return C.total;
+    }
     return L.total;
 }
 
@@ -469,6 +505,56 @@ mha_status_t output_projection_impl(mha_dtype_t dt, const void* w_o, const void*
     return launch_projection(p, W, s, "output projection launch");
 }
 
+// A bf16 problem whose head width the tensor-core kernels do not take: convert the
+// activations, weights and biases to fp32 copies in the workspace, run the fp32
+// forward on them, convert the output back (round to nearest even).
+mha_status_t forward_bf16_on_f32(const void* query, const void* key, const void* value, const void* w_q,
+                                 const void* b_q, const void* w_k, const void* b_k, const void* w_v, const void* b_v,
+                                 const void* w_o, const void* b_o, int B, int L_q, int L_k, int d_model, int h,
+                                 const mha_mask_t* mask, void* out, float* p_attn, void* workspace,
+                                 size_t workspace_bytes, cudaStream_t s) {
+    F32Copies C;
+    f32_copies_of(B, L_q, L_k, d_model, h, &C);
+    if (workspace == nullptr) return fail(MHA_ERR_INVALID_ARG, "workspace is NULL");
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(MHA_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+    if (workspace_bytes < C.total)
+        return fail(MHA_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, C.total);
+    const void* ptrs[13] = {query, key, value, w_q, w_k, w_v, w_o, b_q, b_k, b_v, b_o, out, p_attn};
+    for (const void* ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return fail(MHA_ERR_INVALID_ARG, "bf16 tensors must be 16-byte aligned");
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    using bf = const __nv_bfloat16*;
+    const long qn = static_cast<long>(B) * L_q * d_model, kn = static_cast<long>(B) * L_k * d_model;
+    const long dd = static_cast<long>(d_model) * d_model;
+    float* q32 = reinterpret_cast<float*>(ws + C.q);
+    float* k32 = key == query ? q32 : reinterpret_cast<float*>(ws + C.k);
+    float* v32 = value == key ? k32 : reinterpret_cast<float*>(ws + C.v);
+    float* w32 = reinterpret_cast<float*>(ws + C.w);
+    float* b32 = reinterpret_cast<float*>(ws + C.b);
+    float* o32 = reinterpret_cast<float*>(ws + C.out);
+    cudaError_t e = mha::launch_bf16_to_f32(static_cast<bf>(query), q32, qn, s);
+    if (e == cudaSuccess && key != query) e = mha::launch_bf16_to_f32(static_cast<bf>(key), k32, kn, s);
+    if (e == cudaSuccess && value != key) e = mha::launch_bf16_to_f32(static_cast<bf>(value), v32, kn, s);
+    const void* W[4] = {w_q, w_k, w_v, w_o};
+    const void* bias[4] = {b_q, b_k, b_v, b_o};
+    const float* b_f32[4] = {nullptr, nullptr, nullptr, nullptr};
+    for (int i = 0; i < 4 && e == cudaSuccess; ++i) {
+        e = mha::launch_bf16_to_f32(static_cast<bf>(W[i]), w32 + i * dd, dd, s);
+        if (e == cudaSuccess && bias[i]) {
+            e = mha::launch_bf16_to_f32(static_cast<bf>(bias[i]), b32 + i * d_model, d_model, s);
+            b_f32[i] = b32 + i * d_model;
+        }
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "bf16 to fp32 conversion launch");
+    mha_status_t st = mha_forward(MHA_F32, q32, k32, v32, w32, b_f32[0], w32 + dd, b_f32[1], w32 + 2 * dd, b_f32[2],
+                                  w32 + 3 * dd, b_f32[3], B, L_q, L_k, d_model, h, mask, o32, p_attn, ws, C.q, s);
+    if (st != MHA_OK) return st;
+    e = mha::launch_f32_to_bf16(o32, static_cast<__nv_bfloat16*>(out), qn, s);
+    if (e != cudaSuccess) return cuda_fail(e, "fp32 to bf16 conversion launch");
+    return MHA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -493,11 +579,14 @@ mha_status_t mha_forward(mha_dtype_t dt, const void* query, const void* key, con
                          const mha_mask_t* mask, void* out, float* p_attn, void* workspace, size_t workspace_bytes,
                          void* stream) {
     // Validate everything before enqueueing anything.
-    mha_status_t st = check_sizes(dt, B, L_q, L_k, d_model, h);
+    mha_status_t st = check_sizes(dt, B, L_q, L_k, d_model, h, true);
     if (st != MHA_OK) return st;
     if ((st = check_mask(mask, L_q, L_k)) != MHA_OK) return st;
     if (!query || !key || !value || !w_q || !w_k || !w_v || !w_o || !out)
         return fail(MHA_ERR_INVALID_ARG, "query, key, value, W_q, W_k, W_v, W_o and out must not be NULL");
+    if (dt == MHA_BF16 && !bf16_native_dk(d_model / h))
+        return forward_bf16_on_f32(query, key, value, w_q, b_q, w_k, b_k, w_v, b_v, w_o, b_o, B, L_q, L_k, d_model,
+                                   h, mask, out, p_attn, workspace, workspace_bytes, as_stream(stream));
     Layout L;
     if ((st = check_workspace(dt, B, L_q, L_k, d_model, h, workspace, workspace_bytes, &L)) != MHA_OK) return st;
     if (dt == MHA_BF16) {
