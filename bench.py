@@ -181,36 +181,37 @@ def oracle_sample(workload: str, prefix: int):
 
     Long sequences: one sequence's causal prefix of ``prefix`` tokens (rows
     0..P-1 of a causal output depend only on tokens 0..P-1). Short ones: the
-    first sequence of the batch, whole, with its own mask. Returns
-    (run, flops, tokens, description)."""
+    whole batch of the workload with its masks (a second or two of fp64
+    work). Returns (run, flops, tokens, description)."""
     import oracle
     from transformer_head_scaled_fwd_gb300 import workloads as W
     oracle.build()
     wl = W.WORKLOADS[workload]
-    inp = W.make_inputs(wl, B=1)
-    w = inp.weights
     if wl.Lq > prefix:
         assert wl.causal and wl.self_attn
+        inp = W.make_inputs(wl, B=1)
         x = np.ascontiguousarray(inp.query[:, :prefix])
         q = k = v = x
-        Lq = Lk = prefix
+        Bs, Lq, Lk = 1, prefix, prefix
         vl = None
         desc = f"1 sequence, causal prefix of {prefix} tokens"
     else:
+        inp = W.make_inputs(wl)
         q = np.ascontiguousarray(inp.query)
         k = q if inp.key is inp.query else np.ascontiguousarray(inp.key)
         v = k
-        Lq, Lk = q.shape[1], k.shape[1]
-        vl = None if inp.valid_lens is None else np.ascontiguousarray(inp.valid_lens[:1])
-        desc = f"1 whole sequence (L_q {Lq}, L_k {Lk}) with its mask"
-    proj, attn = algorithmic_flops(1, Lq, Lk, wl.d_model, wl.h, wl.causal, vl)
+        Bs, Lq, Lk = q.shape[0], q.shape[1], k.shape[1]
+        vl = None if inp.valid_lens is None else np.ascontiguousarray(inp.valid_lens)
+        desc = f"the whole workload ({Bs} sequences, L_q {Lq}, L_k {Lk}) with its masks"
+    w = inp.weights
+    proj, attn = algorithmic_flops(Bs, Lq, Lk, wl.d_model, wl.h, wl.causal, vl)
 
     def run():
         oracle.mha_forward(q, k, v, w["w_q"], w["b_q"], w["w_k"], w["b_k"], w["w_v"], w["b_v"], w["w_o"],
                            w["b_o"], wl.h, causal=wl.causal, valid_lens=vl)
 
-    desc += f" of the workload (d_model {wl.d_model}, h {wl.h}), fp64 C oracle, OpenMP"
-    return run, proj + attn, Lq, desc
+    desc += f" (d_model {wl.d_model}, h {wl.h}), fp64 C oracle, OpenMP"
+    return run, proj + attn, Bs * Lq, desc
 
 
 def run_reference(args):
