@@ -37,8 +37,8 @@ DESCRIPTION = {
     "long": "long-sequence causal self-attention B4 L8192 d_model1024 h16 d_k64",
     "long_d128": "long-sequence causal self-attention B4 L8192 d_model1024 h8 d_k128",
 }
-KERNEL_SOURCES = {"qkv_projection_gemm": "gemm_tc.cu", "attention_core": "attn_tc.cu",
-                  "output_projection_gemm": "gemm_tc.cu"}
+KERNEL_SOURCES = {"qkv_projection_gemm": "gemm_tc2.cu", "attention_core": "attn_tc.cu",
+                  "output_projection_gemm": "gemm_tc2.cu"}
 
 
 def source_digest(kernel: str) -> str:

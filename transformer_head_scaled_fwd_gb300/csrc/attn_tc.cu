@@ -38,6 +38,7 @@
 // (128*64 + 256*216 = 63488 <= 384*168 = 64512, the launch total).
 #include <math_constants.h>
 
+#include "launch.h"
 #include "mha_internal.h"
 #include "ptx.cuh"
 
@@ -83,6 +84,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     AttnSmem* sm = reinterpret_cast<AttnSmem*>(base + kOffBar);
+    pdl_trigger();
+    pdl_wait();   // Qh, KVh and the mask parts come from earlier kernels
 
     // Block order: (batch, head) pairs in groups of kHeadGroup, so the CTAs in
     // flight share the K/V of a few heads in L2; inside a group, longest first
@@ -469,8 +472,7 @@ cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t s) {
                                          static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
     const unsigned grid = static_cast<unsigned>(p.q_pairs) * p.B * p.h;
-    attn_bf16_tc_kernel<<<grid, kAttnThreads, kSmemBytes, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(attn_bf16_tc_kernel, dim3(grid), dim3(kAttnThreads), kSmemBytes, s, p);
 }
 
 cudaError_t launch_pattn_bf16(const PattnParams& p, cudaStream_t s) {

@@ -21,6 +21,7 @@
 // allocates tensor memory), 6-7 idle.
 #include <math_constants.h>
 
+#include "launch.h"
 #include "mha_internal.h"
 #include "ptx.cuh"
 
@@ -60,6 +61,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_d128_kernel(const __grid_con
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Smem128* sm = reinterpret_cast<Smem128*>(base + kOffBar);
+    pdl_trigger();
+    pdl_wait();   // Qh, KVh and the mask parts come from earlier kernels
 
     // (batch, head) pairs in groups of kHeadGroup, longest query tiles first
     const int BH = p.B * p.h;
@@ -343,7 +346,8 @@ cudaError_t launch_attn_tc_d128(const AttnParams& p, cudaStream_t s) {
                                          static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
     const unsigned grid = static_cast<unsigned>(p.q_pairs) * p.B * p.h;
-    attn_d128_kernel<<<grid, kThreads, kSmemBytes, s>>>(p);
+    cudaError_t e2 = launch_pdl(attn_d128_kernel, dim3(grid), dim3(kThreads), kSmemBytes, s, p);
+    if (e2 != cudaSuccess) return e2;
     return cudaGetLastError();
 }
 

@@ -27,6 +27,7 @@
 //                       new token in cache_len[b] (or reports a full cache).
 #include <math_constants.h>
 
+#include "launch.h"
 #include "mha_internal.h"
 #include "ptx.cuh"
 
@@ -37,6 +38,8 @@ constexpr int kD = 64;
 constexpr int kWarps = 4;
 
 __global__ void __launch_bounds__(256) kv_append_kernel(const DecodeParams p) {
+    pdl_trigger();
+    pdl_wait();
     const int b = blockIdx.x;
     const int pos = p.cache_len[b];
     if (pos < 0 || pos >= p.L_max) return;   // full cache: nothing appended (reported by the combine)
@@ -66,6 +69,8 @@ __device__ __forceinline__ float warp_sum(float v) {
 __global__ void __launch_bounds__(32 * kWarps) decode_attn_kernel(const DecodeParams p) {
     __shared__ float sm_m[kWarps], sm_l[kWarps];
     __shared__ float sm_o[kWarps][kD];
+    pdl_trigger();
+    pdl_wait();
     const int bh = blockIdx.y;
     const int b = bh / p.h;
     const int head = bh - b * p.h;
@@ -198,6 +203,8 @@ __global__ void __launch_bounds__(32 * kWarps) decode_attn_kernel(const DecodePa
 }
 
 __global__ void __launch_bounds__(kD) decode_combine_kernel(const DecodeParams p) {
+    pdl_trigger();
+    pdl_wait();
     const int bh = blockIdx.x;
     const int b = bh / p.h;
     const int head = bh - b * p.h;
@@ -238,16 +245,13 @@ __global__ void __launch_bounds__(kD) decode_combine_kernel(const DecodeParams p
 }  // namespace
 
 cudaError_t launch_kv_append(const DecodeParams& p, cudaStream_t s) {
-    kv_append_kernel<<<p.B, 256, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(kv_append_kernel, dim3(p.B), dim3(256), 0, s, p);
 }
 
 cudaError_t launch_decode_attention(const DecodeParams& p, cudaStream_t s) {
-    decode_attn_kernel<<<dim3(p.n_split, p.B * p.h), 32 * kWarps, 0, s>>>(p);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(decode_attn_kernel, dim3(p.n_split, p.B * p.h), dim3(32 * kWarps), 0, s, p);
     if (e != cudaSuccess) return e;
-    decode_combine_kernel<<<p.B * p.h, kD, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(decode_combine_kernel, dim3(p.B * p.h), dim3(kD), 0, s, p);
 }
 
 }  // namespace mha

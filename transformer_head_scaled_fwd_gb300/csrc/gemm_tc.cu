@@ -23,6 +23,7 @@
 //              bf16, stage in swizzled shared memory (two slab buffers) and
 //              TMA-store; the accumulator is released as soon as it is read, so
 //              the next tile's MMAs overlap this tile's stores.
+#include "launch.h"
 #include "mha_internal.h"
 #include "ptx.cuh"
 
@@ -108,6 +109,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
     tc_fence_after();
     const uint32_t tmem = sm->tmem_base;
     volatile int* abort_flag = &sm->abort_flag;
+    pdl_trigger();
+    pdl_wait();   // inputs, bias and residual may come from the previous kernel
 
     if (warp == 0) {
         // ---------------- TMA producer
@@ -261,8 +264,7 @@ cudaError_t launch_gemm_tc(const GemmParams& p, int /*max_m_tiles*/, cudaStream_
     long total = 0;
     for (int g = 0; g < p.ngroups; ++g) total += static_cast<long>(p.g[g].m_tiles) * n_tiles;
     const int grid = static_cast<int>(total < sms ? total : sms);
-    gemm_bf16_tc_kernel<<<grid, kGemmThreads, kSmemBytes, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(gemm_bf16_tc_kernel, dim3(grid), dim3(kGemmThreads), kSmemBytes, s, p);
 }
 
 }  // namespace mha

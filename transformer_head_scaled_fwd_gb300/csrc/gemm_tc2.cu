@@ -24,6 +24,7 @@
 // Every wait is bounded; at the end each producer waits for the last releases of
 // its ring and both CTAs meet at a cluster barrier before freeing tensor memory.
 #include "gemm_pair.h"
+#include "launch.h"
 #include "ptx_pair.cuh"
 
 namespace mha {
@@ -128,6 +129,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     const uint32_t tmem = sm->tmem_base;
     volatile int* abort_flag = &sm->abort_flag;
+    pdl_trigger();
+    pdl_wait();   // inputs, bias and residual may come from the previous kernel
 
     if (warp == 0) {
         // ---------------- TMA producer (both CTAs)
@@ -310,8 +313,8 @@ cudaError_t launch_gemm_tc2(const GemmParams& p, cudaStream_t s) {
         units += bn * ((p.g[g].L + 2 * kGemmBM - 1) / (2 * kGemmBM)) * n_tiles;
     }
     const long clusters = units < sms / 2 ? units : sms / 2;
-    gemm_bf16_tc2_kernel<<<static_cast<unsigned>(2 * clusters), kGemmThreads, kSmemBytes, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(gemm_bf16_tc2_kernel, dim3(static_cast<unsigned>(2 * clusters)), dim3(kGemmThreads),
+                      kSmemBytes, s, p);
 }
 
 }  // namespace mha

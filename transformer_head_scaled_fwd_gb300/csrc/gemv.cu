@@ -12,6 +12,8 @@
 // straight into the key / value caches at each sequence's current length (k and v
 // of the step), or plain [M, N].
 #include "gemv.h"
+#include "launch.h"
+#include "ptx.cuh"
 
 namespace mha {
 namespace {
@@ -39,6 +41,8 @@ __global__ void __launch_bounds__(32 * kGemvWarps) gemv_bf16_kernel(const __grid
     const int K = KC * 256;
     const int n0 = blockIdx.x * kGemvFeatures + 2 * warp;   // this warp's features n0, n0 + 1
     const __nv_bfloat16* W = p.w[g];
+    pdl_trigger();
+    pdl_wait();   // x (and the cache lengths) may come from the previous kernel
 
     // the two W rows, all chunks in flight at once (16 bytes per lane per chunk)
     uint4 wv[2][KC];
@@ -132,15 +136,14 @@ cudaError_t launch_gemv_bf16(const GemvParams& p, cudaStream_t s) {
     const size_t smem = static_cast<size_t>(kGemvRows) * p.K * 2;
     dim3 grid((p.N + kGemvFeatures - 1) / kGemvFeatures, p.ngroups);
     switch (kc) {
-        case 1: gemv_bf16_kernel<1><<<grid, 32 * kGemvWarps, smem, s>>>(p); break;
-        case 2: gemv_bf16_kernel<2><<<grid, 32 * kGemvWarps, smem, s>>>(p); break;
-        case 4: gemv_bf16_kernel<4><<<grid, 32 * kGemvWarps, smem, s>>>(p); break;
+        case 1: return launch_pdl(gemv_bf16_kernel<1>, grid, dim3(32 * kGemvWarps), smem, s, p);
+        case 2: return launch_pdl(gemv_bf16_kernel<2>, grid, dim3(32 * kGemvWarps), smem, s, p);
+        case 4: return launch_pdl(gemv_bf16_kernel<4>, grid, dim3(32 * kGemvWarps), smem, s, p);
         case 8: {
             cudaError_t e = cudaFuncSetAttribute(gemv_bf16_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  static_cast<int>(smem));
             if (e != cudaSuccess) return e;
-            gemv_bf16_kernel<8><<<grid, 32 * kGemvWarps, smem, s>>>(p);
-            break;
+            return launch_pdl(gemv_bf16_kernel<8>, grid, dim3(32 * kGemvWarps), smem, s, p);
         }
         default: return cudaErrorInvalidValue;
     }

@@ -118,6 +118,14 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Programmatic dependent launch. pdl_wait(): wait until the grids this one depends on
+// (the earlier work on the stream) have completed and their writes are visible; every
+// thread that reads data an earlier kernel may have written calls it first.
+// pdl_trigger(): let the next grid on the stream be scheduled before this one ends (it
+// still waits for this grid's completion before touching what this grid writes).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Named barrier over `nthreads` threads (ids 1..15; 0 is __syncthreads).
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
