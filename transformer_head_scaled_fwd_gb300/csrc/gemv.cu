@@ -5,8 +5,8 @@
 // the kernel spreads W over many CTAs instead of tiling M: a CTA computes 8
 // output features of one matrix for all rows. Each warp owns 2 features; its
 // lanes stream the two W rows with 16-byte loads and multiply them with the x
-// rows staged in shared memory (16 rows per pass), accumulating 2 x 16 sums in
-// fp32. A 5-step butterfly (reduce-scatter over the 32 lanes) leaves lane l with
+// rows staged in shared memory as fp32 (16 rows per pass), accumulating 2 x 16
+// sums with packed fp32 FMAs. A 5-step butterfly (reduce-scatter over the 32 lanes) leaves lane l with
 // the complete sum of (feature l / 16, row l % 16), which it finishes with the
 // bias and stores as bf16: head-split [planes, M, 64] (the q of the step),
 // straight into the key / value caches at each sequence's current length (k and v
@@ -32,9 +32,12 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
     }
 }
 
-template <int KC>   // K / 256: 16-byte chunks per lane per W row
+template <int KC>   // K / 256: 16-byte chunks of W per lane per W row
 __global__ void __launch_bounds__(32 * kGemvWarps) gemv_bf16_kernel(const __grid_constant__ GemvParams p) {
-    extern __shared__ uint4 xs[];   // [kGemvRows][K / 8] 16-byte chunks of the staged x rows
+    // x rows staged once per pass as fp32, laid out so that lane l's 8 elements of chunk j
+    // of row r are two float4 at ((r * KC + j) * 2 + half) * 32 + l: every ld.shared.v4 of
+    // a warp reads 512 contiguous bytes
+    extern __shared__ float4 xs[];
     const int g = blockIdx.y;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -44,15 +47,18 @@ __global__ void __launch_bounds__(32 * kGemvWarps) gemv_bf16_kernel(const __grid
     pdl_trigger();
     pdl_wait();   // x (and the cache lengths) may come from the previous kernel
 
-    // the two W rows, all chunks in flight at once (16 bytes per lane per chunk)
-    uint4 wv[2][KC];
+    // the two W rows as fp32 pairs, all chunks loaded at once (16 bytes per lane per chunk)
+    float2 wf[2][KC][4];
 #pragma unroll
     for (int f = 0; f < 2; ++f)
 #pragma unroll
         for (int j = 0; j < KC; ++j) {
             const int n = n0 + f;
-            wv[f][j] = n < p.N ? *reinterpret_cast<const uint4*>(W + static_cast<long>(n) * K + (j * 32 + lane) * 8)
-                               : make_uint4(0, 0, 0, 0);
+            const uint4 raw = n < p.N ? *reinterpret_cast<const uint4*>(W + static_cast<long>(n) * K + (j * 32 + lane) * 8)
+                                      : make_uint4(0, 0, 0, 0);
+            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) wf[f][j][e] = __bfloat1622float2(h2[e]);
         }
 
     for (int mb = 0; mb < p.M; mb += kGemvRows) {
@@ -63,34 +69,45 @@ __global__ void __launch_bounds__(32 * kGemvWarps) gemv_bf16_kernel(const __grid
             uint4 t[kPer];
 #pragma unroll
             for (int u = 0; u < kPer; ++u) {
-                const int i = threadIdx.x + u * 32 * kGemvWarps;
+                const int i = threadIdx.x + u * 32 * kGemvWarps;   // chunk i of the 16 rows: row i / (K/8)
                 const int r = i / (K / 8), c = i - r * (K / 8);
                 t[u] = (mb + r < p.M) ? *reinterpret_cast<const uint4*>(p.x + static_cast<long>(mb + r) * K + c * 8)
                                       : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
-            for (int u = 0; u < kPer; ++u) xs[threadIdx.x + u * 32 * kGemvWarps] = t[u];
+            for (int u = 0; u < kPer; ++u) {
+                const int i = threadIdx.x + u * 32 * kGemvWarps;
+                const int r = i / (K / 8), c = i - r * (K / 8);   // c = j * 32 + l
+                const int j = c >> 5, l = c & 31;
+                const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&t[u]);
+                const float2 a = __bfloat1622float2(h2[0]), b = __bfloat1622float2(h2[1]);
+                const float2 cc = __bfloat1622float2(h2[2]), d = __bfloat1622float2(h2[3]);
+                xs[((r * KC + j) * 2 + 0) * 32 + l] = make_float4(a.x, a.y, b.x, b.y);
+                xs[((r * KC + j) * 2 + 1) * 32 + l] = make_float4(cc.x, cc.y, d.x, d.y);
+            }
         }
         __syncthreads();
-        float acc[2 * kGemvRows];   // index f * 16 + row
+        float2 acc2[2 * kGemvRows];   // index f * 16 + row; the two halves of a packed sum
 #pragma unroll
-        for (int i = 0; i < 2 * kGemvRows; ++i) acc[i] = 0.0f;
+        for (int i = 0; i < 2 * kGemvRows; ++i) acc2[i] = make_float2(0.0f, 0.0f);
 #pragma unroll
         for (int j = 0; j < KC; ++j) {
-            float w0[8], w1[8];
-            bf16x8_to_f32(wv[0][j], w0);
-            bf16x8_to_f32(wv[1][j], w1);
 #pragma unroll
             for (int r = 0; r < kGemvRows; ++r) {
-                float xv[8];
-                bf16x8_to_f32(xs[r * (K / 8) + j * 32 + lane], xv);
+                const float4 xa = xs[((r * KC + j) * 2 + 0) * 32 + lane];
+                const float4 xb = xs[((r * KC + j) * 2 + 1) * 32 + lane];
+                const float2 x2[4] = {make_float2(xa.x, xa.y), make_float2(xa.z, xa.w), make_float2(xb.x, xb.y),
+                                      make_float2(xb.z, xb.w)};
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    acc[r] = fmaf(w0[e], xv[e], acc[r]);
-                    acc[kGemvRows + r] = fmaf(w1[e], xv[e], acc[kGemvRows + r]);
+                for (int e = 0; e < 4; ++e) {
+                    acc2[r] = ffma2(wf[0][j][e], x2[e], acc2[r]);
+                    acc2[kGemvRows + r] = ffma2(wf[1][j][e], x2[e], acc2[kGemvRows + r]);
                 }
             }
         }
+        float acc[2 * kGemvRows];
+#pragma unroll
+        for (int i = 0; i < 2 * kGemvRows; ++i) acc[i] = acc2[i].x + acc2[i].y;
         // reduce-scatter: after the step of width s, lane keeps the half of its values
         // selected by (lane & s); at the end acc[0] = total of value index `lane`
 #pragma unroll
@@ -131,23 +148,24 @@ bool gemv_supported(int M, int K) {
     return M >= 1 && M <= kGemvMaxRows && (K == 256 || K == 512 || K == 1024 || K == 2048);
 }
 
+template <int KC>
+cudaError_t launch_kc(const GemvParams& p, dim3 grid, cudaStream_t s) {
+    const size_t smem = static_cast<size_t>(kGemvRows) * KC * 256 * sizeof(float);   // fp32 x rows
+    cudaError_t e = cudaFuncSetAttribute(gemv_bf16_kernel<KC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    return launch_pdl(gemv_bf16_kernel<KC>, grid, dim3(32 * kGemvWarps), smem, s, p);
+}
+
 cudaError_t launch_gemv_bf16(const GemvParams& p, cudaStream_t s) {
-    const int kc = p.K / 256;
-    const size_t smem = static_cast<size_t>(kGemvRows) * p.K * 2;
     dim3 grid((p.N + kGemvFeatures - 1) / kGemvFeatures, p.ngroups);
-    switch (kc) {
-        case 1: return launch_pdl(gemv_bf16_kernel<1>, grid, dim3(32 * kGemvWarps), smem, s, p);
-        case 2: return launch_pdl(gemv_bf16_kernel<2>, grid, dim3(32 * kGemvWarps), smem, s, p);
-        case 4: return launch_pdl(gemv_bf16_kernel<4>, grid, dim3(32 * kGemvWarps), smem, s, p);
-        case 8: {
-            cudaError_t e = cudaFuncSetAttribute(gemv_bf16_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 static_cast<int>(smem));
-            if (e != cudaSuccess) return e;
-            return launch_pdl(gemv_bf16_kernel<8>, grid, dim3(32 * kGemvWarps), smem, s, p);
-        }
+    switch (p.K / 256) {
+        case 1: return launch_kc<1>(p, grid, s);
+        case 2: return launch_kc<2>(p, grid, s);
+        case 4: return launch_kc<4>(p, grid, s);
+        case 8: return launch_kc<8>(p, grid, s);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 }  // namespace mha
