@@ -28,11 +28,13 @@
 //                     by more than 2^8 (lazy: exact, the final O / l uses the
 //                     same m), write P with tcgen05.st.
 //   warp 8            TMA: Q tiles once, K and V tiles through a 4-deep ring.
-//   warps 9 / 10      tcgen05.mma issuers for query tile 0 / 1 (one thread each):
-//                     S_t = Q_t K^T (SS, M=128, N=128), O_t += P_t V (A from
-//                     tensor memory, V MN-major, M=128, N=64). Warp 9 also
-//                     allocates the tensor memory.
-//   warp 11           idle (it completes the third warpgroup).
+//   warp 9            issues S_t = Q_t K^T for both tiles (SS, M=128, N=128)
+//                     and allocates the tensor memory.
+//   warps 10 / 11     issue O_t += P_t V for tile 0 / 1 (A from tensor memory,
+//                     V MN-major, M=128, N=64).
+// The score MMAs have their own issuing thread so that S_t(j+1) enters the
+// tensor pipe as soon as the softmax has loaded S_t(j), instead of queueing
+// behind the P.V MMAs, whose issue the busy pipe holds back.
 // Registers: launched at 168 per thread (384 threads); the third warpgroup
 // drops to 64 and the two softmax warpgroups rise to 216
 // (128*64 + 256*216 = 63488 <= 384*168 = 64512, the launch total).
@@ -131,8 +133,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
         for (int s = 0; s < kAttnStages; ++s) {
             mbar_init(&sm->k_full[s], 1);
             mbar_init(&sm->v_full[s], 1);
-            mbar_init(&sm->k_empty[s], 2);   // both MMA issuers commit every stage
-            mbar_init(&sm->v_empty[s], 2);
+            mbar_init(&sm->k_empty[s], 1);   // the score issuer
+            mbar_init(&sm->v_empty[s], 2);   // both P.V issuers commit every stage
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(&sm->s_full[t], 1);
@@ -178,57 +180,58 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
                 tma_load_3d(&p.kv_map, &sm->v_full[s], base + kOffV + s * kTileBytes, 0, j * kAttnBN, v_slab);
             }
         }
-    } else if (warp == 9 || warp == 10) {
-        // ------------------------------------------------ MMA issuers, one per query tile
-        // Issuer t runs S_t(j) and P_t(j-1).V_{j-1} software-pipelined; the two
-        // issuers' dependent MMA chains interleave in the tensor pipe and each
-        // one's barrier waits overlap the other's MMAs. Both commit every K/V
-        // stage (the *_empty barriers count 2), also for key tiles their own
-        // query tile does not use, after waiting for that stage to be filled.
-        const int t = warp - 9;
+    } else if (warp == 9) {
+        // ------------------------------------------------ score MMAs, both query tiles
         if (lane == 0 && n_all > 0) {
             constexpr uint32_t idesc_s = idesc_bf16(kAttnBM, kAttnBN, false, false);
-            constexpr uint32_t idesc_o = idesc_bf16(kAttnBM, kAttnD, false, true);
-            const uint32_t qa = smem_u32(base + kOffQ) + t * kTileBytes;
             const uint32_t k_addr = smem_u32(base + kOffK);
-            const uint32_t v_addr = smem_u32(base + kOffV);
-            const uint32_t d_s = tmem + kColS + t * 128;
-            const uint32_t a_p = tmem + kColP + t * 64;
-            const uint32_t d_o = tmem + kColO + t * 64;
-            const int n_t = tw[t].n;
-            if (n_t > 0) mbar_wait(&sm->q_full, 0, abort_flag, p.status, 0x203);
-            for (int j = 0; j <= n_all; ++j) {
-                if (j < n_all) {
-                    const int s = j % kAttnStages;
-                    mbar_wait(&sm->k_full[s], (j / kAttnStages) & 1, abort_flag, p.status, 0x204);
-                    if (j < n_t) {
+            mbar_wait(&sm->q_full, 0, abort_flag, p.status, 0x203);
+            for (int j = 0; j < n_all; ++j) {
+                const int s = j % kAttnStages;
+                mbar_wait(&sm->k_full[s], (j / kAttnStages) & 1, abort_flag, p.status, 0x204);
+                const uint32_t ka = k_addr + s * kTileBytes;
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    if (j < tw[t].n) {
                         if (j > 0) mbar_wait(&sm->s_free[t], (j - 1) & 1, abort_flag, p.status, 0x20a);
                         tc_fence_after();
-                        const uint32_t ka = k_addr + s * kTileBytes;
+                        const uint32_t qa = smem_u32(base + kOffQ) + t * kTileBytes;
+                        const uint32_t d_s = tmem + kColS + t * 128;
 #pragma unroll
                         for (int k = 0; k < kAttnD / 16; ++k)
                             mma_ss(d_s, sdesc_sw128(qa + k * 32, 16, 1024), sdesc_sw128(ka + k * 32, 16, 1024),
                                    idesc_s, k > 0);
                         tc_commit(&sm->s_full[t]);
                     }
-                    tc_commit(&sm->k_empty[s]);
                 }
-                if (j >= 1) {
-                    const int jj = j - 1;
-                    const int s = jj % kAttnStages;
-                    mbar_wait(&sm->v_full[s], (jj / kAttnStages) & 1, abort_flag, p.status, 0x205);
-                    if (jj < n_t) {
-                        mbar_wait(&sm->p_full[t], jj & 1, abort_flag, p.status, 0x207);
-                        tc_fence_after();
-                        const uint32_t va = v_addr + s * kTileBytes;
+                tc_commit(&sm->k_empty[s]);
+            }
+        }
+    } else if (warp == 10 || warp == 11) {
+        // ------------------------------------------------ P.V MMAs of query tile t
+        // Both commit every V stage, also for key tiles their own query tile does
+        // not use, after waiting for that stage to be filled.
+        const int t = warp - 10;
+        if (lane == 0 && n_all > 0) {
+            constexpr uint32_t idesc_o = idesc_bf16(kAttnBM, kAttnD, false, true);
+            const uint32_t v_addr = smem_u32(base + kOffV);
+            const uint32_t a_p = tmem + kColP + t * 64;
+            const uint32_t d_o = tmem + kColO + t * 64;
+            const int n_t = tw[t].n;
+            for (int j = 0; j < n_all; ++j) {
+                const int s = j % kAttnStages;
+                mbar_wait(&sm->v_full[s], (j / kAttnStages) & 1, abort_flag, p.status, 0x205);
+                if (j < n_t) {
+                    mbar_wait(&sm->p_full[t], j & 1, abort_flag, p.status, 0x207);
+                    tc_fence_after();
+                    const uint32_t va = v_addr + s * kTileBytes;
 #pragma unroll
-                        for (int k = 0; k < kAttnBN / 16; ++k)
-                            mma_ts(d_o, a_p + k * 8, sdesc_sw128(va + k * 2048, 8192, 1024), idesc_o,
-                                   (jj > 0 || k > 0) ? 1u : 0u);
-                        tc_commit(&sm->pv_done[t]);
-                    }
-                    tc_commit(&sm->v_empty[s]);
+                    for (int k = 0; k < kAttnBN / 16; ++k)
+                        mma_ts(d_o, a_p + k * 8, sdesc_sw128(va + k * 2048, 8192, 1024), idesc_o,
+                               (j > 0 || k > 0) ? 1u : 0u);
+                    tc_commit(&sm->pv_done[t]);
                 }
+                tc_commit(&sm->v_empty[s]);
             }
         }
       }

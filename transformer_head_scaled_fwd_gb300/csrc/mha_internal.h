@@ -55,7 +55,7 @@ constexpr int kAttnBM = 128;       // queries per Q tile
 constexpr int kAttnBN = 128;       // keys per K/V tile
 constexpr int kAttnD = 64;         // head width d_k
 constexpr int kAttnStages = 4;     // K/V ring depth
-constexpr int kAttnThreads = 384;  // 2 softmax warpgroups (one per Q tile) + 1 warpgroup: TMA warp, 2 MMA warps, 1 idle
+constexpr int kAttnThreads = 384;  // 2 softmax warpgroups (one per Q tile) + 1 warpgroup: TMA warp, 3 MMA warps
 
 struct AttnParams {
     CUtensorMap q_map;     // Qh as {64, L_q, B*h}
