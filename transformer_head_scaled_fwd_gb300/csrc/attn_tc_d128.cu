@@ -17,8 +17,10 @@
 // stages (each tile two halves). S = Q K^T is SS-MMA M=128 N=128 (8 k-steps);
 // O += P V takes P from tensor memory and V MN-major with N = 128 (the two
 // 64-wide halves are the descriptor's two MN blocks, LBO apart).
-// Warps: 0-3 softmax (one thread per query row), 4 TMA, 5 MMA issuer (also
-// allocates tensor memory), 6-7 idle.
+// Warps: 0-3 softmax (one thread per query row), 4 TMA, 5 issues the score MMAs
+// (and allocates tensor memory), 6 issues the P.V MMAs, 7 idle. With their own
+// issuing thread the score MMAs of tile j + 1 start as soon as the softmax has
+// released the buffer, instead of queueing behind the P.V MMAs of tile j - 1.
 #include <math_constants.h>
 
 #include "launch.h"
@@ -142,15 +144,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_d128_kernel(const __grid_con
             }
         }
     } else if (warp == 5) {
-        // ------------------------------------------------ MMA issuer
+        // ------------------------------------------------ score MMAs: S(j) = Q K_j^T into buffer j % 2
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16(BM, BN, false, false);
-            constexpr uint32_t idesc_o = idesc_bf16(BM, D, false, true);
             const uint32_t qa = smem_u32(base + kOffQ);
             const uint32_t k_addr = smem_u32(base + kOffK);
-            const uint32_t v_addr = smem_u32(base + kOffV);
-            auto issue_s = [&](int j) {   // S(j) = Q K_j^T into buffer j % 2
+            mbar_wait(&sm->q_full, 0, abort_flag, p.status, 0x403);
+            for (int j = 0; j < n; ++j) {
                 const int s = j % kStages;
+                mbar_wait(&sm->k_full[s], (j / kStages) & 1, abort_flag, p.status, 0x404);
+                // the buffer is free once the softmax has loaded S(j - 2)
+                if (j >= 2) mbar_wait(&sm->s_free[j & 1], ((j - 2) >> 1) & 1, abort_flag, p.status, 0x406);
+                tc_fence_after();
                 const uint32_t ka = k_addr + s * kTile;
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
@@ -160,19 +165,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_d128_kernel(const __grid_con
                 }
                 tc_commit(&sm->s_full[j & 1]);
                 tc_commit(&sm->k_empty[s]);
-            };
-            mbar_wait(&sm->q_full, 0, abort_flag, p.status, 0x403);
-            mbar_wait(&sm->k_full[0], 0, abort_flag, p.status, 0x404);
-            tc_fence_after();
-            issue_s(0);
+            }
+        }
+    } else if (warp == 6) {
+        // ------------------------------------------------ P.V MMAs: O += P(j) V_j
+        if (lane == 0) {
+            constexpr uint32_t idesc_o = idesc_bf16(BM, D, false, true);
+            const uint32_t v_addr = smem_u32(base + kOffV);
             for (int j = 0; j < n; ++j) {
-                if (j + 1 < n) {   // next scores, into the buffer the softmax released at j - 1
-                    const int s1 = (j + 1) % kStages;
-                    mbar_wait(&sm->k_full[s1], ((j + 1) / kStages) & 1, abort_flag, p.status, 0x405);
-                    if (j >= 1) mbar_wait(&sm->s_free[(j + 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.status, 0x406);
-                    tc_fence_after();
-                    issue_s(j + 1);
-                }
                 const int s = j % kStages;
                 mbar_wait(&sm->v_full[s], (j / kStages) & 1, abort_flag, p.status, 0x407);
                 mbar_wait(&sm->p_full, j & 1, abort_flag, p.status, 0x408);
