@@ -195,12 +195,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_d128_kernel(const __grid_con
         const uint32_t o_tmem = tmem + lane_off + kColO;
         float m = -CUDART_INF_F;
         float l = 0.0f;
+        // Scores of the current key tile. The load of the next tile's scores is issued
+        // as soon as the exponentials of this one have consumed u, so that its latency
+        // (and the wait for S(j + 1)) overlaps the P store and the loop turnaround.
+        uint32_t u[128];
+        mbar_wait(&sm->s_full[0], 0, abort_flag, p.status, 0x409);
+        __syncwarp();
+        tc_fence_after();
+        tmem_ld_x128_nowait(tmem + lane_off + kColS, u);
         for (int j = 0; j < n; ++j) {
-            mbar_wait(&sm->s_full[j & 1], (j >> 1) & 1, abort_flag, p.status, 0x409);
-            __syncwarp();
-            tc_fence_after();
-            uint32_t u[128];
-            tmem_ld_x128(tmem + lane_off + kColS + (j & 1) * 128, u);
+            tmem_ld_wait();
             tc_fence_before();
             mbar_arrive(&sm->s_free[j & 1]);
             const int k0 = j * BN;
@@ -272,6 +276,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_d128_kernel(const __grid_con
             }
             const float2 s4 = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
             l += s4.x + s4.y;
+            if (j + 1 < n) {
+                mbar_wait(&sm->s_full[(j + 1) & 1], ((j + 1) >> 1) & 1, abort_flag, p.status, 0x409);
+                __syncwarp();
+                tc_fence_after();
+                tmem_ld_x128_nowait(tmem + lane_off + kColS + ((j + 1) & 1) * 128, u);
+            }
             if (j > 0) {
                 mbar_wait(&sm->pv_done, (j - 1) & 1, abort_flag, p.status, 0x40a);
                 __syncwarp();
