@@ -41,11 +41,18 @@ KERNEL_SOURCES = {"qkv_projection_gemm": "gemm_tc2.cu", "attention_core": "attn_
                   "output_projection_gemm": "gemm_tc2.cu"}
 
 
-def source_digest(kernel: str) -> str:
+def kernel_source(kernel: str, workload: str = WORKLOAD) -> str:
+    """Source file of the kernel that runs `kernel` on `workload` (head width 128 has its own attention)."""
+    if kernel == "attention_core" and workload == "long_d128":
+        return "attn_tc_d128.cu"
+    return KERNEL_SOURCES[kernel]
+
+
+def source_digest(kernel: str, workload: str = WORKLOAD) -> str:
     import hashlib
     csrc = os.path.join(ROOT, "transformer_head_scaled_fwd_gb300", "csrc")
     h = hashlib.sha1()
-    for f in (KERNEL_SOURCES[kernel], "ptx.cuh", "mha_internal.h", "tmem_ldst.inc"):
+    for f in (kernel_source(kernel, workload), "ptx.cuh", "mha_internal.h", "tmem_ldst.inc"):
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -58,7 +65,7 @@ def committed_traffic(kernel: str, workload: str):
     pat = re.compile(r"<!-- bench-traffic kernel=(\S+) workload=(\S+) source_sha1=(\S+) bytes_per_launch=(\d+) -->")
     for f in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
         for m in pat.finditer(open(f).read()):
-            if m.group(1) == kernel and m.group(2) == workload and m.group(3) == source_digest(kernel):
+            if m.group(1) == kernel and m.group(2) == workload and m.group(3) == source_digest(kernel, workload):
                 return int(m.group(4))
     return None
 
@@ -452,7 +459,7 @@ def run_gpu(args):
         "stage_ms": {k2: round(v2, 4) for k2, v2 in shares.items()},
         "attention_core": core,
         "graph": graph_line,
-        "roofline": {"kernel": dom, "source_sha1": source_digest(dom), "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+        "roofline": {"kernel": dom, "source_sha1": source_digest(dom, args.workload), "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_src} bf16_tflops (burst); sustained {peaks.get('bf16_tflops_sustained')}"},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
