@@ -84,6 +84,30 @@ def test_long_causal_sampled_rows():
     assert_close(got[:, rows], ref, "bf16")
 
 
+def test_long_single_sequence_ragged_sampled_rows():
+    """The longest case of the suite: one causal sequence of 32768 tokens (four times the bench
+    length) whose keys stop at a valid length of 30001, so tensor-map coordinates and row offsets run
+    far past those of the bench; sampled query rows include the ones around the valid length and the
+    last row (its allowed keys are the first 30001)."""
+    L = 32768
+    inp = W.random_case(71, 1, L, L, 1024, 16, self_attn=True, bias_scale=0.05)
+    vl = [30001]
+    rows = np.unique(np.concatenate([W.sample_rows(L, 48, seed=9), [30000, 30001, 30002]])).astype(np.int32)
+    got, _ = run_gpu(inp, causal=True, valid_lens=vl)
+    ref = run_oracle(inp, causal=True, valid_lens=vl, rows=rows)
+    assert_close(got[:, rows], ref, "bf16")
+
+
+def test_widest_model_dimension():
+    """d_model 2048 with 32 heads: projection GEMMs with 8 column tiles of 256 and K = 2048,
+    attention over 64 (batch, head) planes, ragged valid lengths."""
+    inp = W.random_case(72, 2, 700, 700, 2048, 32, self_attn=True, bias_scale=0.05)
+    vl = [700, 333]
+    got, _ = run_gpu(inp, causal=True, valid_lens=vl)
+    ref = run_oracle(inp, causal=True, valid_lens=vl)
+    assert_close(got, ref, "bf16")
+
+
 # ------------------------------------------------------------------ edge cases (bf16)
 def test_ragged_cross_attention_distinct_kv_bias_p_attn():
     inp = W.random_case(1, 3, 200, 77, 512, 8, kv_alias=False, bias_scale=0.1)
