@@ -21,7 +21,10 @@
 //                       products and an 8-lane reduce-scatter, keeps an online
 //                       softmax (running max and sum) and accumulates p.V per
 //                       lane over its own keys; the CTA's warps merge and write
-//                       a partial (max, sum, o[64]).
+//                       a partial (max, sum, o[64]). When the projections run on
+//                       the small-M kernel, each CTA first issues a bulk L2 prefetch of
+//                       the start of its chunk, before waiting for them: the cache
+//                       streams in while the projections run.
 //   decode_combine_kernel  merges the partials of a (batch, head), writes its
 //                       64-wide slab of the concatenated context, and counts the
 //                       new token in cache_len[b] (or reports a full cache).
@@ -70,6 +73,22 @@ __global__ void __launch_bounds__(32 * kWarps) decode_attn_kernel(const DecodePa
     __shared__ float sm_m[kWarps], sm_l[kWarps];
     __shared__ float sm_o[kWarps][kD];
     pdl_trigger();
+    if (p.prefetch_keys > 0 && threadIdx.x == 0) {
+        // The first keys and values of this CTA's chunk stream into L2 while the step's
+        // projections still run; the new token's row (written by them) is left out.
+        const int pbh = blockIdx.y;
+        const int pb = pbh / p.h;
+        const int pn = min(max(p.cache_len[pb], 0) + 1, p.L_max);
+        const int pchunk = ((pn + p.n_split - 1) / p.n_split + 31) & ~31;
+        const int pc0 = blockIdx.x * pchunk;
+        const int pc1 = min(pn - 1, pc0 + p.prefetch_keys);
+        if (pc1 > pc0) {
+            const long off = (static_cast<long>(pbh) * p.L_max + pc0) * kD;
+            const uint32_t bytes = static_cast<uint32_t>(pc1 - pc0) * kD * 2;
+            prefetch_l2_bulk(p.k_cache + off, bytes);
+            prefetch_l2_bulk(p.v_cache + off, bytes);
+        }
+    }
     pdl_wait();
     const int bh = blockIdx.y;
     const int b = bh / p.h;

@@ -44,8 +44,10 @@ __global__ void __launch_bounds__(32 * kGemvWarps) gemv_bf16_kernel(const __grid
     const int K = KC * 256;
     const int n0 = blockIdx.x * kGemvFeatures + 2 * warp;   // this warp's features n0, n0 + 1
     const __nv_bfloat16* W = p.w[g];
-    pdl_trigger();
     pdl_wait();   // x (and the cache lengths) may come from the previous kernel
+    // Dependents launch only once every CTA has passed its wait: what the kernels before
+    // this one wrote (the cache lengths) is final when they start.
+    pdl_trigger();
 
     // the two W rows as fp32 pairs, all chunks loaded at once (16 bytes per lane per chunk)
     float2 wf[2][KC][4];

@@ -776,6 +776,13 @@ mha_status_t mha_decode_step(mha_dtype_t dt, const void* x_new, const void* w_q,
     p.scale_log2 = static_cast<float>(1.4426950408889634 / 8.0);
     p.status = device_status_ptr();
     if (!p.status) return fail(MHA_ERR_CUDA, "device status word unavailable");
+    // keys each attention CTA prefetches into L2 while the small-M projections run: an eighth
+    // of its chunk, at most 64 MB over the grid (half of L2)
+    if (gemv) {
+        const long ctas = static_cast<long>(p.n_split) * B * h;
+        const long chunk = (L_max + p.n_split - 1) / p.n_split;
+        p.prefetch_keys = static_cast<int>(std::min<long>(chunk / 8, (64l << 20) / (ctas * 2 * 64 * 2)));
+    }
     const cudaStream_t s = as_stream(stream);
     // 2. (tiled projections only) append k, v at cache_len[b]; 3. attention over the cache,
     // the new token included; 4. merge, and count the new token in cache_len[b]

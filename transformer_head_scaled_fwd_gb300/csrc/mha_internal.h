@@ -139,6 +139,10 @@ struct DecodeParams {
     int B, h, L_max, n_split;
     float scale_log2;
     int* status;
+    // Keys each attention CTA prefetches into L2 before its wait on the step's projections
+    // (0: none). Only set when the kernel before the attention triggers its dependents after
+    // its own wait, so that cache_len is final when the attention starts.
+    int prefetch_keys;
 };
 constexpr int kDecodeMaxSplit = 64;
 cudaError_t launch_kv_append(const DecodeParams& p, cudaStream_t s);
