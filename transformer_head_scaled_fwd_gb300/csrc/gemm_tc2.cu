@@ -56,20 +56,43 @@ struct PairCoord {
     int grp, b, l0, n0;
 };
 
+// True when every group has the same rows (batch items and length), as the Q, K
+// and V projections of one input do.
+__device__ __forceinline__ bool groups_share_rows(const GemmParams& p) {
+    for (int g = 1; g < p.ngroups; ++g)
+        if (p.g[g].L != p.g[0].L || p.g[g].m_tiles != p.g[0].m_tiles || p.g[g].tiles_per_b != p.g[0].tiles_per_b)
+            return false;
+    return true;
+}
+
 // Unit u -> group, batch item, this CTA's first row and the tile's first column.
-// A unit is 256 rows (never straddling a batch item) x 256 columns.
-__device__ __forceinline__ PairCoord pair_coord(const GemmParams& p, int u, int n_tiles, int rank) {
+// A unit is 256 rows (never straddling a batch item) x 256 columns. When the
+// groups share their rows, the units of one row pair are consecutive across all
+// groups (row pair, then group, then column tile), so the clusters in flight read
+// the same rows of the input and each row block comes from DRAM once; otherwise
+// the groups follow one another.
+__device__ __forceinline__ PairCoord pair_coord(const GemmParams& p, int u, int n_tiles, int rank,
+                                                bool shared_rows) {
     int g = 0;
-    for (;;) {
-        const int bn = p.g[g].m_tiles / p.g[g].tiles_per_b;
-        const int units = bn * ((p.g[g].L + 2 * kGemmBM - 1) / (2 * kGemmBM)) * n_tiles;
-        if (u < units || g + 1 >= p.ngroups) break;
-        u -= units;
-        ++g;
+    int pm, nt;
+    if (shared_rows) {
+        const int per_pm = p.ngroups * n_tiles;
+        pm = u / per_pm;
+        const int rem = u - pm * per_pm;
+        g = rem / n_tiles;
+        nt = rem - g * n_tiles;
+    } else {
+        for (;;) {
+            const int bn = p.g[g].m_tiles / p.g[g].tiles_per_b;
+            const int units = bn * ((p.g[g].L + 2 * kGemmBM - 1) / (2 * kGemmBM)) * n_tiles;
+            if (u < units || g + 1 >= p.ngroups) break;
+            u -= units;
+            ++g;
+        }
+        pm = u / n_tiles;
+        nt = u - pm * n_tiles;
     }
     const int ptb = (p.g[g].L + 2 * kGemmBM - 1) / (2 * kGemmBM);
-    const int pm = u / n_tiles;
-    const int nt = u - pm * n_tiles;
     PairCoord c;
     c.grp = g;
     c.b = pm / ptb;
@@ -101,6 +124,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     const int kblocks = p.K / kGemmBK;
     const int n_tiles = (p.N + BN - 1) / BN;
     const int total = pair_units(p, n_tiles);
+    const bool shared_rows = groups_share_rows(p);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -137,7 +161,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         if (lane == 0) {
             int it = 0;   // ring position across tiles
             for (int u = cid; u < total; u += ncl) {
-                const PairCoord c = pair_coord(p, u, n_tiles, rank);
+                const PairCoord c = pair_coord(p, u, n_tiles, rank, shared_rows);
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     const int s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1;
@@ -198,7 +222,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                                               mapa_shared(smem_u32(&sm->acc_empty[1]), 0)};
         int use = 0, slabs_issued = 0;
         for (int u = cid; u < total; u += ncl, ++use) {
-            const PairCoord c = pair_coord(p, u, n_tiles, rank);
+            const PairCoord c = pair_coord(p, u, n_tiles, rank, shared_rows);
             const GemmGroup& G = p.g[c.grp];
             const int acc = use & 1;
             if (G.residual != nullptr && c.l0 + row < G.L) {
