@@ -264,13 +264,15 @@ def cpu_baseline(workload: str, prefix: int):
             "kind": "oracle", "seconds": dt, "sample": f"{runs} runs of {sample}"}
 
 
-def host_pipeline_launches(B: int, L_q: int, L_k: int, self_attn: bool) -> int:
+def host_pipeline_launches(B: int, L_q: int, L_k: int, d_model: int, q_distinct: bool, kv_distinct: bool) -> int:
     """Library kernels one bf16 mha_forward_host call launches: 3 per chunk of sequences
-    (up to 4 chunks), plus one more projection at each end when query, key and value are one
-    host buffer (the first chunk's Q/K/V projection and the last chunk's output projection
-    each run in 2 row windows; one chunk holds both ends when B = 1)."""
-    n = 3 * min(B, 4)
-    if self_attn and L_q == L_k and L_q >= 256:
+    (up to 4 chunks when the host input is at least 32 MiB, else up to 2), plus one more
+    projection at each end when query, key and value are one host buffer (the first chunk's
+    Q/K/V projection and the last chunk's output projection each run in 2 row windows; one
+    chunk holds both ends when B = 1)."""
+    in_bytes = 2 * B * d_model * (L_q + (L_k if q_distinct else 0) + (L_k if kv_distinct else 0))
+    n = 3 * min(B, 4 if in_bytes >= 32 << 20 else 2)
+    if not q_distinct and not kv_distinct and L_q == L_k and L_q >= 256:
         n += 2
     return n
 
@@ -388,7 +390,7 @@ def run_gpu(args):
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
-        per_e2e = host_pipeline_launches(Bn, Lq, Lk, inp.key is inp.query and inp.value is inp.key)
+        per_e2e = host_pipeline_launches(Bn, Lq, Lk, d, inp.key is not inp.query, inp.value is not inp.key)
         for s in range(Wm, Wm + K):
             e2e_step(s)
             launches += per_e2e

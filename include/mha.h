@@ -151,7 +151,9 @@ mha_status_t mha_output_projection(mha_dtype_t dt, const void* w_o, const void* 
  * above. The host buffers should be page-locked for the copies to be
  * asynchronous. `staging` is device memory of at least
  * mha_host_staging_size(...) bytes that receives the activations. The call is
- * pipelined over up to 4 chunks of sequences with library-owned streams (one set
+ * pipelined over chunks of sequences (up to 4 when query, key and value hold
+ * at least 32 MiB of host data together, else up to 2; never more than B) with
+ * library-owned streams (one set
  * per device, created on first use): an upload stream, a download stream and a
  * second compute stream. Chunks alternate between `stream` and the second
  * compute stream when the workspace holds two chunk workspaces (each

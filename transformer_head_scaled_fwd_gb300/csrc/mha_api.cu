@@ -905,7 +905,9 @@ namespace {
 // Per-device resources of the host-buffer entry point: an upload stream, a
 // download stream, a second compute stream and events, created on first use
 // and kept for the life of the process.
-constexpr int kHostChunks = 4;
+constexpr int kHostChunks = 4;                       // chunks of a large call
+constexpr int kHostChunksSmall = 2;                  // chunks of a call with less host input
+constexpr size_t kHostLargeBytes = size_t(32) << 20;  // host input bytes from which a call is large
 constexpr int kHostWindows = 2;   // row windows of the first and the last chunk (self-attention)
 constexpr int kHostUnits = kHostChunks + 2 * kHostWindows;
 struct HostPipe {
@@ -992,7 +994,10 @@ mha_status_t mha_forward_host(mha_dtype_t dt, const void* h_query, const void* h
     // into row windows: the first chunk is uploaded window by window and each window's
     // Q/K/V projection starts as soon as its rows have arrived, and the last chunk's
     // output projection and download run window by window after its attention.
-    const int nch = std::min(B, kHostChunks);
+    // Small calls take fewer chunks: their kernels are latency-bound, so every extra
+    // chunk adds launches that cost more than the copy overlap they buy.
+    const size_t in_bytes = qrow * B + (q_distinct ? krow * B : 0) + (kv_distinct ? krow * B : 0);
+    const int nch = std::min(B, in_bytes >= kHostLargeBytes ? kHostChunks : kHostChunksSmall);
     const int per = (B + nch - 1) / nch;
     Layout Lc;
     layout_of(dt, per, L_q, L_k, d_model, h, &Lc);
