@@ -260,8 +260,9 @@ def test_invalid_arguments_leave_output_untouched():
 
 
 def test_forward_host_uneven_chunks_distinct_kv_and_masks():
-    """Host entry point pipelined over chunks of sequences: 5 sequences -> chunks of 2, 2, 1;
-    key != value != query, per-sequence valid lengths and a per-query dense mask (offset per chunk)."""
+    """Host entry point pipelined over chunks of sequences: 5 sequences, a small call -> chunks of
+    3 and 2; key != value != query, per-sequence valid lengths and a per-query dense mask (offset per
+    chunk)."""
     from transformer_head_scaled_fwd_gb300 import binding
     from gpu_helpers import to_dev
     B, Lq, Lk, d, h = 5, 70, 90, 256, 4
@@ -288,9 +289,10 @@ def test_forward_host_uneven_chunks_distinct_kv_and_masks():
 
 @pytest.mark.parametrize("h,masked", [(8, "causal"), (4, "causal"), (8, "pad_dense")])   # d_k 64 and 128
 def test_forward_host_row_windows(h, masked):
-    """Self-attention through the host entry point: each sequence chunk's projections and
-    copies are cut into row windows (here [0, 256) and [256, 640)), three chunks on two
-    compute streams. The result equals the device path bit for bit and matches the oracle."""
+    """Self-attention through the host entry point: the first chunk's projections and uploads
+    and the last chunk's output projection and downloads are cut into row windows (here
+    [0, 256) and [256, 640)); a small call, so two chunks (2 and 1 sequences) on two compute
+    streams. The result equals the device path bit for bit and matches the oracle."""
     from transformer_head_scaled_fwd_gb300 import binding
     from gpu_helpers import to_dev
     B, L, d = 3, 640, 512
@@ -321,6 +323,36 @@ def test_forward_host_row_windows(h, masked):
     rows = [0, 1, 255, 256, 257, 511, 512, 639]
     ref = run_oracle(inp, rows=rows, **kw)
     assert_close(hout.double().numpy()[:, rows], ref, "bf16")
+
+
+def test_forward_host_large_call_four_chunks():
+    """A call with at least 32 MiB of host input is pipelined over four chunks of sequences:
+    5 sequences of 3328 tokens at d_model 1024 (34 MB) -> chunks of 2, 2, 1, the first and the
+    last cut into row windows. Bit-equal to the device path; the last (one-sequence) chunk's
+    sampled rows match the oracle."""
+    from transformer_head_scaled_fwd_gb300 import binding
+    from gpu_helpers import to_dev
+    B, L, d, h = 5, 3328, 1024, 16
+    assert 2 * B * L * d >= 32 << 20
+    inp = W.random_case(140, B, L, L, d, h, self_attn=True, bias_scale=0.1)
+    dev_out, _ = run_gpu(inp, causal=True)
+    dt = torch.bfloat16
+    hq = torch.from_numpy(inp.query).to(dt).pin_memory()
+    hout = torch.full((B, L, d), 7.0, dtype=dt).pin_memory()
+    Wd = {n: to_dev(a, dt) for n, a in inp.weights.items()}
+    staging = torch.empty(binding.host_staging_size(binding.MHA_BF16, B, L, L, d, False, False),
+                          dtype=torch.uint8, device="cuda")
+    ws = torch.empty(binding.workspace_size(binding.MHA_BF16, B, L, L, d, h), dtype=torch.uint8, device="cuda")
+    binding.mha_forward_host(hq, hq, hq, Wd["w_q"], Wd["b_q"], Wd["w_k"], Wd["b_k"], Wd["w_v"], Wd["b_v"],
+                             Wd["w_o"], Wd["b_o"], h, h_out=hout, staging=staging, workspace=ws,
+                             mask=binding.make_mask(causal=True))
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(hout.double().numpy(), dev_out)
+    q4 = np.ascontiguousarray(inp.query[4:5])
+    last = W.Inputs(inp.wl, q4, q4, q4, inp.weights)
+    rows = [0, 1, 1663, 3327]
+    ref = run_oracle(last, causal=True, rows=rows)
+    assert_close(hout.double().numpy()[4:5, rows], ref, "bf16")
 
 
 @pytest.mark.parametrize("d,h", [(256, 8), (384, 4), (512, 2)])   # d_k 32, 96, 256
