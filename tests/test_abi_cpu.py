@@ -96,6 +96,21 @@ def test_validation_without_gpu(lib):
     assert rc == binding.MHA_ERR_INVALID_ARG                                       # null query
 
 
+def test_size_limits_without_gpu(lib):
+    """The largest problems: activations beyond 4e9 elements, or more than 1e15 query/key pairs
+    over all heads, are refused as UNSUPPORTED before anything reaches the GPU (32-bit tile
+    indices); a problem just inside the limits gets past the size check (and here stops at
+    the workspace check, which the caller's 1 GB does not satisfy)."""
+    big = 1 << 30
+    assert _call_forward(lib, B_=64, Lq=1 << 20, Lk=1 << 20, d=1024, h=16, ws=big) == binding.MHA_ERR_UNSUPPORTED
+    assert b"too large" in lib.mha_last_error()
+    # activations inside the limit, 1.2e15 query/key pairs outside it
+    assert _call_forward(lib, B_=1, Lq=60_000_000, Lk=20_000_000, d=64, h=1, ws=big) == binding.MHA_ERR_UNSUPPORTED
+    assert _call_forward(lib, B_=1, Lq=1 << 20, Lk=1 << 20, d=1024, h=16, ws=big) == binding.MHA_ERR_INVALID_ARG
+    assert b"workspace too small" in lib.mha_last_error()
+    assert binding.workspace_size(binding.MHA_BF16, 1, 1 << 20, 1 << 20, 1024, 16) > big
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(ImportError):
         binding._lib = None
