@@ -27,7 +27,10 @@
 //                     apply the -1e9 fill, update (m, l), rescale O when m grows
 //                     by more than 2^8 (lazy: exact, the final O / l uses the
 //                     same m), write P with tcgen05.st.
-//   warp 8            TMA: Q tiles once, K and V tiles through a 4-deep ring.
+//   warp 8            TMA: K and V tiles through a 4-deep ring (Q and the ring's
+//                     first four K/V tiles are issued by thread 0 right after it
+//                     has initialised the barriers, before the tensor-memory
+//                     allocation and the register split).
 //   warp 9            issues S_t = Q_t K^T for both tiles (SS, M=128, N=128)
 //                     and allocates the tensor memory.
 //   warps 10 / 11     issue O_t += P_t V for tile 0 / 1 (A from tensor memory,
@@ -144,8 +147,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
         }
         sm->abort_flag = 0;
         fence_barrier_init();
-        tma_prefetch_desc(&p.q_map);
-        tma_prefetch_desc(&p.kv_map);
+        // The first loads leave now, before tensor memory is allocated and the warps
+        // take their register budgets: Q and the first kAttnStages K/V tiles.
+        const uint32_t qbytes = (tw[0].n > 0 ? kTileBytes : 0) + (tw[1].n > 0 ? kTileBytes : 0);
+        mbar_arrive_expect_tx(&sm->q_full, qbytes);
+        if (tw[0].n > 0) tma_load_3d(&p.q_map, &sm->q_full, base + kOffQ, 0, q0, q_slab);
+        if (tw[1].n > 0) tma_load_3d(&p.q_map, &sm->q_full, base + kOffQ + kTileBytes, 0, q0 + kAttnBM, q_slab);
+        for (int j = 0; j < n_all && j < kAttnStages; ++j) {
+            mbar_arrive_expect_tx(&sm->k_full[j], kTileBytes);
+            tma_load_3d(&p.kv_map, &sm->k_full[j], base + kOffK + j * kTileBytes, 0, j * kAttnBN, k_slab);
+            mbar_arrive_expect_tx(&sm->v_full[j], kTileBytes);
+            tma_load_3d(&p.kv_map, &sm->v_full[j], base + kOffV + j * kTileBytes, 0, j * kAttnBN, v_slab);
+        }
         tma_prefetch_desc(&p.ctx_map);
     }
     if (warp == 9) {
@@ -165,11 +178,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
       if (warp == 8) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
-            uint32_t qbytes = (tw[0].n > 0 ? kTileBytes : 0) + (tw[1].n > 0 ? kTileBytes : 0);
-            mbar_arrive_expect_tx(&sm->q_full, qbytes);
-            if (tw[0].n > 0) tma_load_3d(&p.q_map, &sm->q_full, base + kOffQ, 0, q0, q_slab);
-            if (tw[1].n > 0) tma_load_3d(&p.q_map, &sm->q_full, base + kOffQ + kTileBytes, 0, q0 + kAttnBM, q_slab);
-            for (int j = 0; j < n_all; ++j) {
+            // Q and the first ring's tiles were issued during set-up
+            for (int j = kAttnStages; j < n_all; ++j) {
                 const int s = j % kAttnStages;
                 const uint32_t ph = (j / kAttnStages) & 1;
                 mbar_wait(&sm->k_empty[s], ph ^ 1, abort_flag, p.status, 0x201);
