@@ -85,6 +85,12 @@ struct TileWork {
     bool active;    // query tile has rows < L_q
 };
 
+// kShortKeys: the instance for short key ranges (L_k <= kShortKeysMax), where most key
+// tiles are cut by the causal or valid-length mask and take the one-select fill
+// below; long key ranges use the instance without that branch in the hot loop.
+constexpr int kShortKeysMax = 1024;
+
+template <bool kShortKeys>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __grid_constant__ AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -267,6 +273,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
         const int n = tw[t].n;
         float m = -CUDART_INF_F;
         float l = 0.0f;
+        const uint32_t fill_raw = __float_as_uint(kMaskedLog2 / p.scale_log2);
 
         for (int j = 0; j < n; ++j) {
             mbar_wait(&sm->s_full[t], j & 1, abort_flag, p.status, 0x208);
@@ -283,7 +290,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
             // (scale > 0, so max commutes with it); edge tiles are rewritten in
             // log2 units with the fill applied, and use scale 1.
             float sc = p.scale_log2;
-            if (edge) {
+            if (kShortKeys && edge && can_skip && k0 + kAttnBN <= p.Lk) {
+                // Only the causal / valid-length parts cut this tile, and every row keeps an
+                // allowed key in every visited tile: a masked key gets a raw score that,
+                // scaled like a full tile, is the -1e9 fill, and its weight underflows to
+                // zero exactly as the fill's does.
+                const int lim = min(vl, p.causal ? qi + 1 : p.Lk) - k0;
+#pragma unroll
+                for (int c = 0; c < 128; ++c)
+                    if (c >= lim) u[c] = fill_raw;
+            } else if (edge) {
                 // keys c < lim pass the causal and valid-length parts; c >= oob are past L_k
                 const int lim = min(vl, p.causal ? qi + 1 : p.Lk) - k0;
                 const int oob = p.Lk - k0;
@@ -481,11 +497,13 @@ __global__ void __launch_bounds__(kPKeys) pattn_bf16_kernel(const PattnParams p)
 size_t attn_tc_smem_bytes() { return kSmemBytes; }
 
 cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t s) {
-    cudaError_t e = cudaFuncSetAttribute(attn_bf16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const bool short_keys = p.Lk <= kShortKeysMax;
+    auto* kern = short_keys ? attn_bf16_tc_kernel<true> : attn_bf16_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
     const unsigned grid = static_cast<unsigned>(p.q_pairs) * p.B * p.h;
-    return launch_pdl(attn_bf16_tc_kernel, dim3(grid), dim3(kAttnThreads), kSmemBytes, s, p);
+    return launch_pdl(kern, dim3(grid), dim3(kAttnThreads), kSmemBytes, s, p);
 }
 
 cudaError_t launch_pattn_bf16(const PattnParams& p, cudaStream_t s) {
