@@ -154,6 +154,35 @@ def test_dense_mask(mq):
     assert_close(gp, rp, "bf16", "p_attn")
 
 
+@pytest.mark.parametrize("Lk", [1024, 1100])
+def test_masks_on_both_sides_of_the_short_key_threshold(Lk):
+    """The d_k = 64 kernel has one instance for key ranges up to 1024 and one for longer ones;
+    each handles valid lengths (including 0: uniform rows), a ragged key tail and a dense mask."""
+    B, Lq = 3, 200
+    inp = W.random_case(44 + Lk, B, Lq, Lk, 256, 4, bias_scale=0.1)
+    vl = [Lk, 0, 333]
+    rng = np.random.default_rng(45)
+    got, _ = run_gpu(inp, valid_lens=vl)
+    ref = run_oracle(inp, valid_lens=vl)
+    assert_close(got, ref, "bf16")
+    dense = (rng.random((B, 1, Lk)) < 0.8).astype(np.uint8)
+    got, gp = run_gpu(inp, valid_lens=vl, dense=dense, want_p_attn=True)
+    ref, rp = run_oracle(inp, valid_lens=vl, dense=dense, want_p_attn=True)
+    assert_close(got, ref, "bf16")
+    assert_close(gp, rp, "bf16", "p_attn")
+    np.testing.assert_allclose(gp[1], 1.0 / Lk, rtol=1e-5, atol=0)
+
+
+@pytest.mark.parametrize("L", [1024, 1152])
+def test_causal_padding_on_both_sides_of_the_short_key_threshold(L):
+    inp = W.random_case(46 + L, 2, L, L, 256, 4, self_attn=True, bias_scale=0.1)
+    vl = [L, 517]
+    rows = [0, 1, 127, 128, 516, 517, 700, L - 1]
+    got, _ = run_gpu(inp, causal=True, valid_lens=vl)
+    ref = run_oracle(inp, causal=True, valid_lens=vl, rows=rows)
+    assert_close(got[:, rows], ref, "bf16")
+
+
 def test_dense_mask_with_causal_and_padding():
     B, L = 2, 260
     inp = W.random_case(42, B, L, L, 256, 4, self_attn=True)
