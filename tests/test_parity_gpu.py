@@ -203,6 +203,24 @@ def test_odd_head_counts(h):
     assert_close(got, ref, "bf16")
 
 
+@pytest.mark.parametrize("B,h,Lq,Lk", [(1, 3, 128, 128), (3, 1, 100, 300), (5, 2, 77, 77), (2, 8, 128, 640)])
+def test_two_pairs_per_cta_for_short_queries(B, h, Lq, Lk):
+    """L_q <= 128 (with L_k <= 1024): a CTA's two query tiles serve two (batch, head) pairs,
+    each with its own K/V stages; an odd pair count leaves the last CTA's second tile idle.
+    Per-pair valid lengths (one of them 0: uniform rows), causal when square, p_attn."""
+    d = 64 * h
+    inp = W.random_case(60 + 7 * B + h, B, Lq, Lk, d, h, bias_scale=0.1, self_attn=(Lq == Lk))
+    vl = [max(1, (Lk * (i + 1)) // (B + 1)) for i in range(B)]
+    if B >= 3:
+        vl[1] = 0
+    causal = Lq == Lk
+    got, gp = run_gpu(inp, causal=causal, valid_lens=vl, want_p_attn=True)
+    ref, rp = run_oracle(inp, causal=causal, valid_lens=vl, want_p_attn=True)
+    assert_close(got, ref, "bf16")
+    assert_close(gp, rp, "bf16", "p_attn")
+    np.testing.assert_allclose(gp.sum(-1), 1.0, atol=ROWSUM_TOL)
+
+
 def test_stage_entry_points_equal_forward():
     inp = W.random_case(60, 2, 256, 256, 512, 8, self_attn=True)
     a, _ = run_gpu(inp, causal=True)

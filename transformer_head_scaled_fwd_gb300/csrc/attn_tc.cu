@@ -13,7 +13,8 @@
 // the accumulated output rescaled when m grows), which is an exact rewrite of
 // softmax-then-matmul: the L_q x L_k score matrix never leaves the chip.
 //
-// CTA = two 128-row query tiles (t = 0, 1) of one (batch, head); key tiles of 128.
+// CTA = two 128-row query tiles (t = 0, 1) of one (batch, head); key tiles of 128
+// (when L_q <= 128 the two tiles belong to two consecutive (batch, head) pairs).
 // Tensor memory (512 columns, no aliasing):
 //   S_0 [0,128)  S_1 [128,256)   fp32 scores
 //   P_0 [256,320) P_1 [320,384)  bf16 weights, two per column (A operand of P.V)
@@ -89,8 +90,12 @@ struct TileWork {
 // tiles are cut by the causal or valid-length mask and take the one-select fill
 // below; long key ranges use the instance without that branch in the hot loop.
 constexpr int kShortKeysMax = 1024;
+// kTwo: the instance for query ranges of one tile (L_q <= 128, with short key
+// ranges): the CTA's second query tile takes the next (batch, head) pair instead of
+// staying idle, each pair with its own K/V ring stages (tile t uses the stages of
+// parity t), so the launch has half as many CTAs.
 
-template <bool kShortKeys>
+template <bool kShortKeys, bool kTwo>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __grid_constant__ AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -104,14 +109,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
     const int BH = p.B * p.h;
     const int QP = p.q_pairs;
     const int idx = static_cast<int>(blockIdx.x);
-    const int grp = idx / (kHeadGroup * QP);
-    const int g_heads = min(kHeadGroup, BH - grp * kHeadGroup);
-    const int r = idx - grp * kHeadGroup * QP;
-    const int qp = QP - 1 - r / g_heads;
-    const int bh = grp * kHeadGroup + r % g_heads;
+    int qp, bh;
+    if constexpr (kTwo) {
+        qp = 0;
+        bh = 2 * idx;
+    } else {
+        const int grp = idx / (kHeadGroup * QP);
+        const int g_heads = min(kHeadGroup, BH - grp * kHeadGroup);
+        const int r = idx - grp * kHeadGroup * QP;
+        qp = QP - 1 - r / g_heads;
+        bh = grp * kHeadGroup + r % g_heads;
+    }
     const int b = bh / p.h;
     const int head = bh - b * p.h;
     const int q0 = qp * 2 * kAttnBM;
+    // two-head instance: (batch, head) pair of query tile 1
+    const bool two_on = kTwo && bh + 1 < BH;
+    const int bh1 = two_on ? bh + 1 : bh;
+    const int b1 = bh1 / p.h;
+    const int head1 = bh1 - b1 * p.h;
 
     // Key range. With at least one allowed key per row (valid length >= 1 and
     // no dense mask), key tiles that are fully masked for every row of a query
@@ -120,13 +136,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
     int vl = p.Lk;
     if (p.valid_lens != nullptr) vl = min(max(p.valid_lens[b], 0), p.Lk);
     const bool can_skip = (p.dense == nullptr) && (vl >= 1);
+    int vl1 = vl;
+    if (kTwo && p.valid_lens != nullptr) vl1 = min(max(p.valid_lens[b1], 0), p.Lk);
+    const bool can_skip1 = (p.dense == nullptr) && (vl1 >= 1);
     TileWork tw[2];
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-        const int qt0 = q0 + t * kAttnBM;
-        tw[t].active = qt0 < p.Lq;
-        int kend = can_skip ? vl : p.Lk;
-        if (can_skip && p.causal) kend = min(kend, qt0 + kAttnBM);
+        const int qt0 = kTwo ? 0 : q0 + t * kAttnBM;
+        const int vlt = (kTwo && t == 1) ? vl1 : vl;
+        const bool skt = (kTwo && t == 1) ? can_skip1 : can_skip;
+        tw[t].active = qt0 < p.Lq && (!kTwo || t == 0 || two_on);
+        int kend = skt ? vlt : p.Lk;
+        if (skt && p.causal) kend = min(kend, qt0 + kAttnBM);
         tw[t].n = tw[t].active ? (kend + kAttnBN - 1) / kAttnBN : 0;
     }
     const int n_all = max(tw[0].n, tw[1].n);
@@ -136,6 +157,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
     const int q_slab = b * p.h + head;
     const int k_slab = b * 2 * p.h + head;
     const int v_slab = k_slab + p.h;
+    const int q_slab1 = b1 * p.h + head1;
+    const int k_slab1 = b1 * 2 * p.h + head1;
+    const int v_slab1 = k_slab1 + p.h;
+    // two-head instance: stage use g = 2 j + t holds key tile j of query tile t's pair
+    auto load_kv2 = [&](int g) {
+        const int t = g & 1, j = g >> 1, s = g % kAttnStages;
+        mbar_arrive_expect_tx(&sm->k_full[s], kTileBytes);
+        tma_load_3d(&p.kv_map, &sm->k_full[s], base + kOffK + s * kTileBytes, 0, j * kAttnBN, t ? k_slab1 : k_slab);
+        mbar_arrive_expect_tx(&sm->v_full[s], kTileBytes);
+        tma_load_3d(&p.kv_map, &sm->v_full[s], base + kOffV + s * kTileBytes, 0, j * kAttnBN, t ? v_slab1 : v_slab);
+    };
 
     if (threadIdx.x == 0) {
         mbar_init(&sm->q_full, 1);
@@ -143,7 +175,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
             mbar_init(&sm->k_full[s], 1);
             mbar_init(&sm->v_full[s], 1);
             mbar_init(&sm->k_empty[s], 1);   // the score issuer
-            mbar_init(&sm->v_empty[s], 2);   // both P.V issuers commit every stage
+            mbar_init(&sm->v_empty[s], kTwo ? 1 : 2);   // both P.V issuers commit every stage (kTwo: its own)
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(&sm->s_full[t], 1);
@@ -158,12 +190,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
         const uint32_t qbytes = (tw[0].n > 0 ? kTileBytes : 0) + (tw[1].n > 0 ? kTileBytes : 0);
         mbar_arrive_expect_tx(&sm->q_full, qbytes);
         if (tw[0].n > 0) tma_load_3d(&p.q_map, &sm->q_full, base + kOffQ, 0, q0, q_slab);
-        if (tw[1].n > 0) tma_load_3d(&p.q_map, &sm->q_full, base + kOffQ + kTileBytes, 0, q0 + kAttnBM, q_slab);
-        for (int j = 0; j < n_all && j < kAttnStages; ++j) {
-            mbar_arrive_expect_tx(&sm->k_full[j], kTileBytes);
-            tma_load_3d(&p.kv_map, &sm->k_full[j], base + kOffK + j * kTileBytes, 0, j * kAttnBN, k_slab);
-            mbar_arrive_expect_tx(&sm->v_full[j], kTileBytes);
-            tma_load_3d(&p.kv_map, &sm->v_full[j], base + kOffV + j * kTileBytes, 0, j * kAttnBN, v_slab);
+        if (tw[1].n > 0)
+            tma_load_3d(&p.q_map, &sm->q_full, base + kOffQ + kTileBytes, 0, kTwo ? 0 : q0 + kAttnBM,
+                        kTwo ? q_slab1 : q_slab);
+        if constexpr (kTwo) {
+            for (int g = 0; g < kAttnStages && (g >> 1) < n_all; ++g)
+                if (tw[g & 1].active) load_kv2(g);
+        } else {
+            for (int j = 0; j < n_all && j < kAttnStages; ++j) {
+                mbar_arrive_expect_tx(&sm->k_full[j], kTileBytes);
+                tma_load_3d(&p.kv_map, &sm->k_full[j], base + kOffK + j * kTileBytes, 0, j * kAttnBN, k_slab);
+                mbar_arrive_expect_tx(&sm->v_full[j], kTileBytes);
+                tma_load_3d(&p.kv_map, &sm->v_full[j], base + kOffV + j * kTileBytes, 0, j * kAttnBN, v_slab);
+            }
         }
         tma_prefetch_desc(&p.ctx_map);
     }
@@ -183,7 +222,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
       regs_dec<64>();
       if (warp == 8) {
         // ------------------------------------------------ TMA producer
-        if (lane == 0) {
+        if (lane == 0 && kTwo) {
+            // Q and the first ring's tiles were issued during set-up
+            for (int g = kAttnStages; (g >> 1) < n_all; ++g) {
+                if (!tw[g & 1].active) continue;
+                const int s = g % kAttnStages;
+                const uint32_t ph = (g / kAttnStages) & 1;
+                mbar_wait(&sm->k_empty[s], ph ^ 1, abort_flag, p.status, 0x201);
+                mbar_wait(&sm->v_empty[s], ph ^ 1, abort_flag, p.status, 0x202);
+                load_kv2(g);
+            }
+        } else if (lane == 0) {
             // Q and the first ring's tiles were issued during set-up
             for (int j = kAttnStages; j < n_all; ++j) {
                 const int s = j % kAttnStages;
@@ -198,7 +247,32 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
         }
     } else if (warp == 9) {
         // ------------------------------------------------ score MMAs, both query tiles
-        if (lane == 0 && n_all > 0) {
+        if (lane == 0 && n_all > 0 && kTwo) {
+            constexpr uint32_t idesc_s = idesc_bf16(kAttnBM, kAttnBN, false, false);
+            const uint32_t k_addr = smem_u32(base + kOffK);
+            mbar_wait(&sm->q_full, 0, abort_flag, p.status, 0x203);
+            for (int j = 0; j < n_all; ++j) {
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    if (!tw[t].active) continue;
+                    const int g = 2 * j + t, s = g % kAttnStages;
+                    mbar_wait(&sm->k_full[s], (g / kAttnStages) & 1, abort_flag, p.status, 0x204);
+                    if (j < tw[t].n) {
+                        if (j > 0) mbar_wait(&sm->s_free[t], (j - 1) & 1, abort_flag, p.status, 0x20a);
+                        tc_fence_after();
+                        const uint32_t qa = smem_u32(base + kOffQ) + t * kTileBytes;
+                        const uint32_t ka = k_addr + s * kTileBytes;
+                        const uint32_t d_s = tmem + kColS + t * 128;
+#pragma unroll
+                        for (int k = 0; k < kAttnD / 16; ++k)
+                            mma_ss(d_s, sdesc_sw128(qa + k * 32, 16, 1024), sdesc_sw128(ka + k * 32, 16, 1024),
+                                   idesc_s, k > 0);
+                        tc_commit(&sm->s_full[t]);
+                    }
+                    tc_commit(&sm->k_empty[s]);
+                }
+            }
+        } else if (lane == 0 && n_all > 0) {
             constexpr uint32_t idesc_s = idesc_bf16(kAttnBM, kAttnBN, false, false);
             const uint32_t k_addr = smem_u32(base + kOffK);
             mbar_wait(&sm->q_full, 0, abort_flag, p.status, 0x203);
@@ -235,8 +309,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
             const uint32_t d_o = tmem + kColO + t * 64;
             const int n_t = tw[t].n;
             for (int j = 0; j < n_all; ++j) {
-                const int s = j % kAttnStages;
-                mbar_wait(&sm->v_full[s], (j / kAttnStages) & 1, abort_flag, p.status, 0x205);
+                if (kTwo && !tw[t].active) break;   // kTwo: this tile's stages only
+                const int g = kTwo ? 2 * j + t : j;
+                const int s = g % kAttnStages;
+                mbar_wait(&sm->v_full[s], (g / kAttnStages) & 1, abort_flag, p.status, 0x205);
                 if (j < n_t) {
                     mbar_wait(&sm->p_full[t], j & 1, abort_flag, p.status, 0x207);
                     tc_fence_after();
@@ -264,8 +340,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
         const int t = warp >> 2;
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
-        const int qt0 = q0 + t * kAttnBM;
+        const int qt0 = kTwo ? 0 : q0 + t * kAttnBM;
         const int qi = qt0 + row;
+        // this query tile's (batch, head) pair (the CTA's, or the second one of kTwo)
+        const bool second = kTwo && t == 1;
+        const int tb = second ? b1 : b;
+        const int thead = second ? head1 : head;
+        const int tvl = second ? vl1 : vl;
+        const bool tskip = second ? can_skip1 : can_skip;
+        const int tq_slab = second ? q_slab1 : q_slab;
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t s_tmem = tmem + lane_off + kColS + t * 128;
         const uint32_t p_tmem = tmem + lane_off + kColP + t * 64;
@@ -284,24 +367,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
             tc_fence_before();
             mbar_arrive(&sm->s_free[t]);   // S_t may now be overwritten by S_t(j+1)
             const int k0 = j * kAttnBN;
-            const bool edge = (p.dense != nullptr) || (k0 + kAttnBN > vl) ||
+            const bool edge = (p.dense != nullptr) || (k0 + kAttnBN > tvl) ||
                               (p.causal && k0 + kAttnBN - 1 > qt0);
             // Full tiles keep raw scores and fold the scale into the exponent
             // (scale > 0, so max commutes with it); edge tiles are rewritten in
             // log2 units with the fill applied, and use scale 1.
             float sc = p.scale_log2;
-            if (kShortKeys && edge && can_skip && k0 + kAttnBN <= p.Lk) {
+            if (kShortKeys && edge && tskip && k0 + kAttnBN <= p.Lk) {
                 // Only the causal / valid-length parts cut this tile, and every row keeps an
                 // allowed key in every visited tile: a masked key gets a raw score that,
                 // scaled like a full tile, is the -1e9 fill, and its weight underflows to
                 // zero exactly as the fill's does.
-                const int lim = min(vl, p.causal ? qi + 1 : p.Lk) - k0;
+                const int lim = min(tvl, p.causal ? qi + 1 : p.Lk) - k0;
 #pragma unroll
                 for (int c = 0; c < 128; ++c)
                     if (c >= lim) u[c] = fill_raw;
             } else if (edge) {
                 // keys c < lim pass the causal and valid-length parts; c >= oob are past L_k
-                const int lim = min(vl, p.causal ? qi + 1 : p.Lk) - k0;
+                const int lim = min(tvl, p.causal ? qi + 1 : p.Lk) - k0;
                 const int oob = p.Lk - k0;
 #pragma unroll
                 for (int c = 0; c < 128; ++c) {
@@ -311,7 +394,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
                 if (p.dense != nullptr && qi < p.Lq) {
                     const long mrow = (p.dense_mq == 1) ? 0 : qi;
                     const long mq = (p.dense_mq == 1) ? 1 : p.Lq;
-                    const uint8_t* mr = p.dense + (static_cast<long>(b) * mq + mrow) * p.Lk + k0;
+                    const uint8_t* mr = p.dense + (static_cast<long>(tb) * mq + mrow) * p.Lk + k0;
                     uint32_t keep[4];   // bit c: dense mask allows key k0 + c
 #pragma unroll
                     for (int w = 0; w < 4; ++w) {
@@ -417,13 +500,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
                 st_shared_v4(stage + ((ch ^ (row & 7)) << 4), w[0], w[1], w[2], w[3]);
             }
             if (p.stats != nullptr && qi < p.Lq) {
-                float2* st = reinterpret_cast<float2*>(p.stats) + (static_cast<long>(q_slab) * p.Lq + qi);
+                float2* st = reinterpret_cast<float2*>(p.stats) + (static_cast<long>(tq_slab) * p.Lq + qi);
                 *st = make_float2(m, l);
             }
             fence_proxy_async_smem();
             named_bar_sync(1 + t, kAttnBM);
             if (row == 0 && !*abort_flag) {
-                tma_store_3d(&p.ctx_map, base + kOffQ + t * kTileBytes, head * kAttnD, qt0, b);
+                tma_store_3d(&p.ctx_map, base + kOffQ + t * kTileBytes, thead * kAttnD, qt0, tb);
                 tma_store_commit();
                 tma_store_wait_all();
             }
@@ -498,11 +581,14 @@ size_t attn_tc_smem_bytes() { return kSmemBytes; }
 
 cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t s) {
     const bool short_keys = p.Lk <= kShortKeysMax;
-    auto* kern = short_keys ? attn_bf16_tc_kernel<true> : attn_bf16_tc_kernel<false>;
+    const long BH = static_cast<long>(p.B) * p.h;
+    const bool two = short_keys && p.Lq <= kAttnBM && BH >= 2;
+    auto* kern = two ? attn_bf16_tc_kernel<true, true>
+                     : short_keys ? attn_bf16_tc_kernel<true, false> : attn_bf16_tc_kernel<false, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
-    const unsigned grid = static_cast<unsigned>(p.q_pairs) * p.B * p.h;
+    const unsigned grid = two ? static_cast<unsigned>((BH + 1) / 2) : static_cast<unsigned>(p.q_pairs) * p.B * p.h;
     return launch_pdl(kern, dim3(grid), dim3(kAttnThreads), kSmemBytes, s, p);
 }
 
