@@ -71,6 +71,15 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, int tile, i
     return c;
 }
 
+// The 64 bias values of the output columns [n, n + 64) as eight 16-byte vectors
+// (zero without a bias, and for columns at or past N).
+__device__ __forceinline__ void load_bias_slab(const __nv_bfloat16* bias, int n, int N, uint4 (&dst)[8]) {
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch)
+        dst[ch] = (bias != nullptr && n + ch * 8 < N) ? *reinterpret_cast<const uint4*>(bias + n + ch * 8)
+                                                      : make_uint4(0, 0, 0, 0);
+}
+
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -172,6 +181,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
                 const int lines = min(BN, p.N - c.n0) / 64;
                 for (int q = 0; q < lines; ++q) asm volatile("prefetch.global.L2 [%0];" ::"l"(rp + q * 128));
             }
+            // the first slab's bias is requested before the accumulator is ready, each next
+            // slab's while the current one is converted: its load latency stays hidden
+            uint4 bias_cur[8];
+            load_bias_slab(G.bias, c.n0, p.N, bias_cur);
             mbar_wait(&sm->acc_full[acc], (use >> 1) & 1, abort_flag, p.status, 0x103);
             __syncwarp();
             tc_fence_after();
@@ -179,6 +192,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
 #pragma unroll 1
             for (int slab = 0; slab < BN / 64; ++slab) {
                 const int n = c.n0 + slab * 64;
+                uint4 bias_next[8];
+                load_bias_slab(G.bias, slab + 1 < BN / 64 ? n + 64 : p.N, p.N, bias_next);
                 uint32_t v[64];
                 tmem_ld_x64(t_row + slab * 64, v);
                 if (slab == BN / 64 - 1) {
@@ -186,7 +201,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
                     tc_fence_before();
                     mbar_arrive(&sm->acc_empty[acc]);
                 }
-                if (n >= p.N) continue;   // uniform across the CTA
+                if (n >= p.N) {   // uniform across the CTA
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) bias_cur[ch] = bias_next[ch];
+                    continue;
+                }
                 const int sb = slabs_issued & 1;
                 // the TMA store that last used this staging buffer must have read it
                 if (issuer && slabs_issued >= 2) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
@@ -201,13 +220,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
                     uint4 rv = make_uint4(0, 0, 0, 0);
                     if (has_res) rv = *reinterpret_cast<const uint4*>(res_row + ch * 8);
                     const __nv_bfloat162* r2 = reinterpret_cast<const __nv_bfloat162*>(&rv);
+                    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&bias_cur[ch]);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int cc = ch * 8 + 2 * e;
-                        const float b0 = G.bias ? __bfloat162float(G.bias[n + cc]) : 0.0f;
-                        const float b1 = G.bias ? __bfloat162float(G.bias[n + cc + 1]) : 0.0f;
-                        float y0 = __uint_as_float(v[cc]) + b0;
-                        float y1 = __uint_as_float(v[cc + 1]) + b1;
+                        const float2 bf = __bfloat1622float2(b2[e]);
+                        float y0 = __uint_as_float(v[cc]) + bf.x;
+                        float y1 = __uint_as_float(v[cc + 1]) + bf.y;
                         if (p.relu) {
                             y0 = fmaxf(y0, 0.0f);
                             y1 = fmaxf(y1, 0.0f);
@@ -233,6 +252,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
                     tma_store_commit();
                 }
                 ++slabs_issued;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) bias_cur[ch] = bias_next[ch];
             }
         }
         if (issuer) tma_store_wait_all();

@@ -110,6 +110,15 @@ __device__ __forceinline__ int pair_units(const GemmParams& p, int n_tiles) {
     return total;
 }
 
+// The 64 bias values of the output columns [n, n + 64) as eight 16-byte vectors
+// (zero without a bias, and for columns at or past N).
+__device__ __forceinline__ void load_bias_slab(const __nv_bfloat16* bias, int n, int N, uint4 (&dst)[8]) {
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch)
+        dst[ch] = (bias != nullptr && n + ch * 8 < N) ? *reinterpret_cast<const uint4*>(bias + n + ch * 8)
+                                                      : make_uint4(0, 0, 0, 0);
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_tc2_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -232,6 +241,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                 const int lines = min(BN, p.N - c.n0) / 64;
                 for (int q = 0; q < lines; ++q) asm volatile("prefetch.global.L2 [%0];" ::"l"(rp + q * 128));
             }
+            // the first slab's bias is requested before the accumulator is ready, each next
+            // slab's while the current one is converted: its load latency stays hidden
+            uint4 bias_cur[8];
+            load_bias_slab(G.bias, c.n0, p.N, bias_cur);
             mbar_wait(&sm->acc_full[acc], (use >> 1) & 1, abort_flag, p.status, 0x113);
             __syncwarp();
             tc_fence_after();
@@ -239,6 +252,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 #pragma unroll 1
             for (int slab = 0; slab < BN / 64; ++slab) {
                 const int n = c.n0 + slab * 64;
+                uint4 bias_next[8];
+                load_bias_slab(G.bias, slab + 1 < BN / 64 ? n + 64 : p.N, p.N, bias_next);
                 uint32_t v[64];
                 tmem_ld_x64(t_row + slab * 64, v);
                 if (slab == BN / 64 - 1) {
@@ -252,7 +267,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                             mbar_arrive_remote(leader_acc_empty[acc]);
                     }
                 }
-                if (n >= p.N) continue;   // uniform across the CTA
+                if (n >= p.N) {   // uniform across the CTA
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) bias_cur[ch] = bias_next[ch];
+                    continue;
+                }
                 const int sb = slabs_issued & 1;
                 // the TMA store that last used this staging buffer must have read it
                 if (issuer && slabs_issued >= 2) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
@@ -267,9 +286,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                     uint4 rv = make_uint4(0, 0, 0, 0);
                     if (has_res) rv = *reinterpret_cast<const uint4*>(res_row + ch * 8);
                     const __nv_bfloat162* r2 = reinterpret_cast<const __nv_bfloat162*>(&rv);
-                    uint4 bv = make_uint4(0, 0, 0, 0);
-                    if (G.bias) bv = *reinterpret_cast<const uint4*>(G.bias + n + ch * 8);
-                    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&bv);
+                    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&bias_cur[ch]);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int cc = ch * 8 + 2 * e;
@@ -301,6 +318,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                     tma_store_commit();
                 }
                 ++slabs_issued;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) bias_cur[ch] = bias_next[ch];
             }
         }
         if (issuer) tma_store_wait_all();
