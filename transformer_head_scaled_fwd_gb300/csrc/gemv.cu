@@ -64,6 +64,13 @@ __global__ void __launch_bounds__(32 * kGemvWarps) gemv_bf16_kernel(const __grid
         }
 
     for (int mb = 0; mb < p.M; mb += kGemvRows) {
+        // After the butterfly lane l holds (feature l / 16, row l % 16): its bias and, for
+        // the cache writes, its sequence's cache length are requested now so that their
+        // latency overlaps the staging and the products.
+        const int n_out = n0 + (lane >> 4);
+        const int m_out = mb + (lane & 15);
+        const float bias_out = (p.bias[g] != nullptr && n_out < p.N) ? __bfloat162float(p.bias[g][n_out]) : 0.0f;
+        const int pos_out = (g > 0 && p.k_cache != nullptr && m_out < p.M) ? p.cache_len[m_out] : -1;
         __syncthreads();   // the previous pass has finished reading xs
         {
             // every thread's 16-byte loads of the 16 x rows in flight together
@@ -122,13 +129,12 @@ __global__ void __launch_bounds__(32 * kGemvWarps) gemv_bf16_kernel(const __grid
                 acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
             }
         }
-        const int n = n0 + (lane >> 4);
-        const int m = mb + (lane & 15);
+        const int n = n_out;
+        const int m = m_out;
         if (n < p.N && m < p.M) {
-            float y = acc[0];
-            if (p.bias[g]) y += __bfloat162float(p.bias[g][n]);
+            const float y = p.bias[g] != nullptr ? acc[0] + bias_out : acc[0];
             if (g > 0 && p.k_cache != nullptr) {   // the step's key / value: straight into the cache
-                const int pos = p.cache_len[m];
+                const int pos = pos_out;
                 if (pos >= 0 && pos < p.L_max)
                     (g == 1 ? p.k_cache : p.v_cache)[((static_cast<long>(m) * (p.N / 64) + n / 64) * p.L_max + pos) *
                                                           64 + (n & 63)] = __float2bfloat16_rn(y);
