@@ -23,6 +23,7 @@
 //              bf16, stage in swizzled shared memory (two slab buffers) and
 //              TMA-store; the accumulator is released as soon as it is read, so
 //              the next tile's MMAs overlap this tile's stores.
+#include "gemm_bias.cuh"
 #include "launch.h"
 #include "mha_internal.h"
 #include "ptx.cuh"
@@ -69,15 +70,6 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, int tile, i
     c.l0 = (mt - c.b * p.g[g].tiles_per_b) * kGemmBM;
     c.n0 = nt * BN;
     return c;
-}
-
-// The 64 bias values of the output columns [n, n + 64) as eight 16-byte vectors
-// (zero without a bias, and for columns at or past N).
-__device__ __forceinline__ void load_bias_slab(const __nv_bfloat16* bias, int n, int N, uint4 (&dst)[8]) {
-#pragma unroll
-    for (int ch = 0; ch < 8; ++ch)
-        dst[ch] = (bias != nullptr && n + ch * 8 < N) ? *reinterpret_cast<const uint4*>(bias + n + ch * 8)
-                                                      : make_uint4(0, 0, 0, 0);
 }
 
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __grid_constant__ GemmParams p) {

@@ -23,6 +23,7 @@
 //              per warp of both CTAs: count 8).
 // Every wait is bounded; at the end each producer waits for the last releases of
 // its ring and both CTAs meet at a cluster barrier before freeing tensor memory.
+#include "gemm_bias.cuh"
 #include "gemm_pair.h"
 #include "launch.h"
 #include "ptx_pair.cuh"
@@ -108,15 +109,6 @@ __device__ __forceinline__ int pair_units(const GemmParams& p, int n_tiles) {
         total += bn * ((p.g[g].L + 2 * kGemmBM - 1) / (2 * kGemmBM)) * n_tiles;
     }
     return total;
-}
-
-// The 64 bias values of the output columns [n, n + 64) as eight 16-byte vectors
-// (zero without a bias, and for columns at or past N).
-__device__ __forceinline__ void load_bias_slab(const __nv_bfloat16* bias, int n, int N, uint4 (&dst)[8]) {
-#pragma unroll
-    for (int ch = 0; ch < 8; ++ch)
-        dst[ch] = (bias != nullptr && n + ch * 8 < N) ? *reinterpret_cast<const uint4*>(bias + n + ch * 8)
-                                                      : make_uint4(0, 0, 0, 0);
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
