@@ -199,6 +199,10 @@ mha_status_t mha_forward_host(mha_dtype_t dt,
  *     d_model=1024 does not).
  *   - The first call on each device looks up the scratch address with that
  *     device current; make that first call before any stream capture begins.
+ *     The address belongs to the device's current CUDA context: after the
+ *     context is destroyed and re-created (e.g. cudaDeviceReset), the next
+ *     call sees the new context and looks the address up again, so that call
+ *     too belongs outside stream capture.
  *   - All calls on a device share the one scratch area: calls whose work
  *     overlaps on the GPU (other streams, other host threads) race and corrupt
  *     each other. Serialise them, e.g. on one stream.

@@ -1,5 +1,5 @@
-"""bf16 tensor-core path with head width d_k = 128 vs the fp64 oracle (the survey's
-next row: heads wider than 64, e.g. d_model 1024 with h = 8)."""
+"""bf16 tensor-core path with head width d_k = 128 vs the fp64 oracle (heads wider
+than 64, e.g. d_model 1024 with h = 8)."""
 import numpy as np
 import pytest
 

@@ -414,3 +414,35 @@ def test_bf16_other_head_widths(d, h):
     assert_close(got, ref, "bf16")
     np.testing.assert_allclose(pa.sum(-1), 1.0, atol=1e-3)
     assert np.abs(pa - ref_pa).max() < 5e-3
+
+
+@pytest.mark.parametrize("d, h", [(512, 16), (512, 8)])
+def test_query_is_a_prefix_of_key_buffer(d, h):
+    """query and key start at the same address but the key is longer (L_k > L_q): the
+    query is the first B*L_q*d_model elements of the key buffer, read as [B, L_q, d_model].
+    Both the fp32-copy route (d_k = 32) and the tensor-core route (d_k = 64) must read every
+    key row from the key buffer, not from a conversion sized for the query."""
+    import torch as T
+    from transformer_head_scaled_fwd_gb300 import binding
+    B, Lq, Lk = 2, 48, 112
+    inp = W.random_case(140 + h, B, Lk, Lk, d, h, self_attn=True, bias_scale=0.1)
+    kv = inp.query                                          # [B, L_k, d]
+    q = np.ascontiguousarray(kv.reshape(-1)[:B * Lq * d].reshape(B, Lq, d))
+    dev = lambda a: T.from_numpy(np.ascontiguousarray(a)).cuda().to(T.bfloat16)
+    kv_d = dev(kv)
+    q_d = kv_d.reshape(-1)[:B * Lq * d].view(B, Lq, d)
+    assert q_d.data_ptr() == kv_d.data_ptr()
+    w = {n: dev(a) for n, a in inp.weights.items()}
+    vl = [112, 57]
+    mask = binding.make_mask(False, T.tensor(vl, dtype=T.int32, device="cuda"), None)
+    ws = T.empty(binding.workspace_size(binding.MHA_BF16, B, Lq, Lk, d, h), dtype=T.uint8, device="cuda")
+    # the workspace starts dirty, as a reused caller buffer would
+    ws.fill_(0x7f)
+    out = T.empty(B, Lq, d, dtype=T.bfloat16, device="cuda")
+    binding.mha_forward(q_d, kv_d, kv_d, w["w_q"], w["b_q"], w["w_k"], w["b_k"], w["w_v"], w["b_v"],
+                        w["w_o"], w["b_o"], h, out=out, workspace=ws, mask=mask)
+    T.cuda.synchronize()
+    assert binding.mha_check_device_status(reset=True) == 0
+    case = W.Inputs(inp.wl, q, kv, kv, inp.weights)
+    ref = run_oracle(case, valid_lens=np.asarray(vl, np.int32))
+    assert_close(out.double().cpu().numpy(), ref, "bf16")

@@ -3,8 +3,8 @@
 // Same computation as attn_tc.cu ("The Annotated Transformer", section
 // "Attention", attention(): scores / sqrt(d_k), masked_fill(mask == 0, -1e9),
 // softmax over keys, P.V; the head's output written into its slab of the
-// concatenated context), for the wider heads the survey lists next (e.g.
-// d_model 1024 with h = 8). With d_k = 128 each score costs twice the tensor
+// concatenated context), for heads of width 128 (e.g. d_model 1024 with
+// h = 8). With d_k = 128 each score costs twice the tensor
 // work of d_k = 64 for the same exponential, so one 128-row query tile per CTA
 // keeps the tensor pipe busy:
 //

@@ -527,14 +527,18 @@ mha_status_t forward_bf16_on_f32(const void* query, const void* key, const void*
     using bf = const __nv_bfloat16*;
     const long qn = static_cast<long>(B) * L_q * d_model, kn = static_cast<long>(B) * L_k * d_model;
     const long dd = static_cast<long>(d_model) * d_model;
+    // A shared input is converted once, but only when both views cover the same rows: a
+    // key that starts at the query's address but is longer (L_k > L_q) has rows the query's
+    // conversion never touches, so it gets its own copy.
     float* q32 = reinterpret_cast<float*>(ws + C.q);
-    float* k32 = key == query ? q32 : reinterpret_cast<float*>(ws + C.k);
+    const bool k_is_q = key == query && L_k == L_q;
+    float* k32 = k_is_q ? q32 : reinterpret_cast<float*>(ws + C.k);
     float* v32 = value == key ? k32 : reinterpret_cast<float*>(ws + C.v);
     float* w32 = reinterpret_cast<float*>(ws + C.w);
     float* b32 = reinterpret_cast<float*>(ws + C.b);
     float* o32 = reinterpret_cast<float*>(ws + C.out);
     cudaError_t e = mha::launch_bf16_to_f32(static_cast<bf>(query), q32, qn, s);
-    if (e == cudaSuccess && key != query) e = mha::launch_bf16_to_f32(static_cast<bf>(key), k32, kn, s);
+    if (e == cudaSuccess && !k_is_q) e = mha::launch_bf16_to_f32(static_cast<bf>(key), k32, kn, s);
     if (e == cudaSuccess && value != key) e = mha::launch_bf16_to_f32(static_cast<bf>(value), v32, kn, s);
     const void* W[4] = {w_q, w_k, w_v, w_o};
     const void* bias[4] = {b_q, b_k, b_v, b_o};
