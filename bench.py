@@ -36,6 +36,7 @@ DESCRIPTION = {
     "xattn": "encoder-decoder attention B16 Lq256 Lk320 d_model1024 h16 d_k64, memory as key/value, padding U{160..320}",
     "long": "long-sequence causal self-attention B4 L8192 d_model1024 h16 d_k64",
     "long_d128": "long-sequence causal self-attention B4 L8192 d_model1024 h8 d_k128",
+    "tiny": "tiny fp32 self-attention B2 L10 d_model512 h8 d_k64, key padding valid lens [10, 7]",
 }
 KERNEL_SOURCES = {"qkv_projection_gemm": "gemm_tc2.cu", "attention_core": "attn_tc.cu",
                   "output_projection_gemm": "gemm_tc2.cu"}
@@ -277,13 +278,129 @@ def host_pipeline_launches(B: int, L_q: int, L_k: int, d_model: int, q_distinct:
     return n
 
 
+class WorkloadRun:
+    """One workload on the current GPU, inputs resident in HBM: the whole sublayer through the
+    public entry point mha_forward (one call per step), and the three stage entry points timed
+    one by one with CUDA events between them (the per-kernel breakdown and the attention core)."""
+
+    def __init__(self, name, rank=0, device=0):
+        import torch
+        from transformer_head_scaled_fwd_gb300 import binding
+        from transformer_head_scaled_fwd_gb300 import workloads as W
+        self.torch, self.binding = torch, binding
+        self.name = name
+        self.wl = wl = W.WORKLOADS[name]
+        self.inp = inp = rank_inputs(wl, rank)
+        self.tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+        self.dt = binding.MHA_BF16 if wl.dtype == "bf16" else binding.MHA_F32
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(f"cuda:{device}").to(self.tdt)
+        self.q = dev(inp.query)
+        self.k = self.q if inp.key is inp.query else dev(inp.key)
+        self.v = self.k if inp.value is inp.key else dev(inp.value)
+        self.Wt = {n: dev(a) for n, a in inp.weights.items()}
+        self.B, self.Lq, self.d = inp.query.shape
+        self.Lk = inp.key.shape[1]
+        self.h = wl.h
+        vl = None if inp.valid_lens is None else torch.from_numpy(inp.valid_lens).cuda()
+        self.vl = vl
+        self.mask = binding.make_mask(wl.causal, vl, None)
+        self.ws = torch.empty(binding.workspace_size(self.dt, self.B, self.Lq, self.Lk, self.d, self.h),
+                              dtype=torch.uint8, device="cuda")
+        self.out = torch.empty(self.B, self.Lq, self.d, dtype=self.tdt, device="cuda")
+        self.proj, self.attn = algorithmic_flops(self.B, self.Lq, self.Lk, self.d, self.h, wl.causal,
+                                                 inp.valid_lens)
+        self.flops = self.proj + self.attn
+        # launches of one mha_forward: bf16 runs three kernels; fp32 runs the Q and the K/V
+        # projections as two launches, then the attention and the output projection
+        self.launches_per_step = 3 if wl.dtype == "bf16" else 4
+        # attention-core algorithmic bytes: Q, K, V read once, ctx written
+        es = 2 if wl.dtype == "bf16" else 4
+        self.core_bytes = es * (self.B * self.Lq * self.d + 2 * self.B * self.Lk * self.d + self.B * self.Lq * self.d)
+
+    def forward(self, stream):
+        W = self.Wt
+        self.binding.mha_forward(self.q, self.k, self.v, W["w_q"], W["b_q"], W["w_k"], W["b_k"], W["w_v"],
+                                 W["b_v"], W["w_o"], W["b_o"], self.h, out=self.out, workspace=self.ws,
+                                 mask=self.mask, stream=stream)
+
+    def stages(self, stream, marks):
+        W, b = self.Wt, self.binding
+        b.mha_qkv_projection(self.q, self.k, self.v, W["w_q"], W["b_q"], W["w_k"], W["b_k"], W["w_v"], W["b_v"],
+                             self.h, workspace=self.ws, stream=stream)
+        marks[1].record(stream)
+        b.mha_attention_core(self.dt, self.B, self.Lq, self.Lk, self.d, self.h, workspace=self.ws,
+                             mask=self.mask, stream=stream)
+        marks[2].record(stream)
+        b.mha_output_projection(W["w_o"], W["b_o"], self.B, self.Lq, self.Lk, self.h, out=self.out,
+                                workspace=self.ws, stream=stream)
+
+    def time_steps(self, steps, warmup, flush, stream):
+        """Mean and median ms of `steps` mha_forward calls (L2 flushed before each, outside the events)."""
+        torch = self.torch
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps + warmup)]
+        for s in range(warmup + steps):
+            flush.zero_()
+            ev[s][0].record(stream)
+            self.forward(stream)
+            ev[s][1].record(stream)
+        torch.cuda.synchronize()
+        ms = [a.elapsed_time(b) for a, b in ev[warmup:]]
+        return ms
+
+    def time_stages(self, steps, warmup, flush, stream):
+        """Per-stage ms from the three stage entry points with events between them."""
+        torch = self.torch
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps + warmup)]
+        for s in range(warmup + steps):
+            flush.zero_()
+            evs[s][0].record(stream)
+            self.stages(stream, evs[s])
+            evs[s][3].record(stream)
+        torch.cuda.synchronize()
+        t = evs[warmup:]
+        return ([e[0].elapsed_time(e[1]) for e in t], [e[1].elapsed_time(e[2]) for e in t],
+                [e[2].elapsed_time(e[3]) for e in t])
+
+    def core_record(self, att_ms, peaks):
+        m = statistics.mean(att_ms)
+        return {"ms": m, "median_ms": statistics.median(att_ms), "tflops": self.attn / (m * 1e-3) / 1e12,
+                "algorithmic_bytes": self.core_bytes, "gbs": self.core_bytes / (m * 1e-3) / 1e9,
+                "hbm_frac": self.core_bytes / (m * 1e-3) / 1e9 / float(peaks["hbm_gbs"]),
+                "bf16_frac": self.attn / (m * 1e-3) / 1e12 / float(peaks["bf16_tflops"])}
+
+
+def per_workload_records(names, peaks, flush, stream, steps=50, warmup=5):
+    """Short records of the other workloads (one GPU, rank 0): step time through mha_forward,
+    TFLOP/s, and the attention core's time, GB/s and fractions of the measured peaks."""
+    out, launches = {}, 0
+    for name in names:
+        r = WorkloadRun(name)
+        ms = r.time_steps(steps, warmup, flush, stream)
+        q_ms, a_ms, o_ms = r.time_stages(steps, warmup, flush, stream)
+        # mha_forward calls and stage triples, warm-up included (the fp32 stages also launch 4 kernels)
+        launches += 2 * r.launches_per_step * (steps + warmup)
+        mean = statistics.mean(ms)
+        core = r.core_record(a_ms, peaks)
+        bound = "tensor" if name.startswith("long") else ("latency" if r.wl.dtype == "f32" else "hbm")
+        frac = core["bf16_frac"] if bound == "tensor" else (core["hbm_frac"] if bound == "hbm" else None)
+        out[name] = {"workload": DESCRIPTION[name], "dtype": r.wl.dtype, "steps": steps,
+                     "ms_per_step": mean, "median_ms_per_step": statistics.median(ms),
+                     "tflops": r.flops / (mean * 1e-3) / 1e12, "tokens_per_s": r.B * r.Lq / (mean * 1e-3),
+                     "stage_ms": {"qkv_projection_gemm": round(statistics.mean(q_ms), 5),
+                                  "attention_core": round(statistics.mean(a_ms), 5),
+                                  "output_projection_gemm": round(statistics.mean(o_ms), 5)},
+                     "attention_core": {**core, "bound": bound, "frac": frac}}
+        del r
+    return out, launches
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
 
     from transformer_head_scaled_fwd_gb300 import binding
     from transformer_head_scaled_fwd_gb300 import build as B
-    from transformer_head_scaled_fwd_gb300 import workloads as W
 
     world, rank, local = dist_setup()
     if world > 1:
@@ -298,40 +415,16 @@ def run_gpu(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.workload, args.ref_prefix)
 
-    wl = W.WORKLOADS[args.workload]
     # weak scaling: every rank runs the full per-GPU batch with its own seed
-    inp = rank_inputs(wl, rank)
-    dt = torch.bfloat16
-    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(f"cuda:{local}").to(dt)
-    q = dev(inp.query)
-    k = q if inp.key is inp.query else dev(inp.key)
-    v = k if inp.value is inp.key else dev(inp.value)
-    Wt = {n: dev(a) for n, a in inp.weights.items()}
-    Bn, Lq, d = inp.query.shape
-    Lk = inp.key.shape[1]
-    h = wl.h
-    vl = None if inp.valid_lens is None else torch.from_numpy(inp.valid_lens).cuda()
-    mask = binding.make_mask(wl.causal, vl, None)
-    ws = torch.empty(binding.workspace_size(binding.MHA_BF16, Bn, Lq, Lk, d, h), dtype=torch.uint8, device="cuda")
-    out = torch.empty(Bn, Lq, d, dtype=dt, device="cuda")
+    r = WorkloadRun(args.workload, rank, local)
+    wl, inp = r.wl, r.inp
+    dt = r.tdt
+    Bn, Lq, Lk, d, h = r.B, r.Lq, r.Lk, r.d, r.h
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
-    proj, attn = algorithmic_flops(Bn, Lq, Lk, d, h, wl.causal, inp.valid_lens)
-    flops = proj + attn
-
-    def step(st=None, marks=None):
-        st = stream if st is None else st
-        binding.mha_qkv_projection(q, k, v, Wt["w_q"], Wt["b_q"], Wt["w_k"], Wt["b_k"], Wt["w_v"], Wt["b_v"], h,
-                                   workspace=ws, stream=st)
-        if marks is not None:
-            marks[1].record(st)
-        binding.mha_attention_core(binding.MHA_BF16, Bn, Lq, Lk, d, h, workspace=ws, mask=mask, stream=st)
-        if marks is not None:
-            marks[2].record(st)
-        binding.mha_output_projection(Wt["w_o"], Wt["b_o"], Bn, Lq, Lk, h, out=out, workspace=ws, stream=st)
-
+    proj, attn, flops = r.proj, r.attn, r.flops
     K, Wm = args.steps, args.warmup
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K + Wm)]
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K + Wm)]
 
     # ---- end to end through the host-buffer entry point (pinned host in/out)
     hq = torch.from_numpy(np.ascontiguousarray(inp.query)).to(dt).pin_memory()
@@ -343,6 +436,7 @@ def run_gpu(args):
     h2d = hq.numel() * 2 + (hk.numel() * 2 if hk is not hq else 0) + (hv.numel() * 2 if hv is not hk else 0)
     d2h = hout.numel() * 2
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Wm + K)]
+    Wt, mask, ws = r.Wt, r.mask, r.ws
 
     def e2e_step(s):
         flush.zero_()
@@ -352,22 +446,24 @@ def run_gpu(args):
                                  stream=stream)
         e2e_ev[s][1].record(stream)
 
+    def dev_step(s):
+        flush.zero_()                      # evict L2 between steps (outside the events)
+        evs[s][0].record(stream)
+        r.forward(stream)
+        evs[s][1].record(stream)
+
     # warm-up (untimed): device steps and host-buffer steps
     for s in range(Wm):
-        ev = evs[s]
-        flush.zero_()
-        ev[0].record(stream)
-        step(marks=ev)
-        ev[3].record(stream)
+        dev_step(s)
         e2e_step(s)
     torch.cuda.synchronize()
 
-    # ---- the same three launches captured once in a CUDA graph (replayed below)
+    # ---- the same call captured once in a CUDA graph (replayed below)
     graph = None
     if not args.no_graph:
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
-            step(st=torch.cuda.current_stream())
+            r.forward(torch.cuda.current_stream())
         for s in range(Wm):
             flush.zero_()
             graph.replay()
@@ -375,21 +471,21 @@ def run_gpu(args):
     g_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
 
     launches = 0
+    stage_steps = min(K, 100)
     with ClockSampler(local) as clk:
         time.sleep(0.3)                        # let the sampler start
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
         for s in range(Wm, Wm + K):
-            ev = evs[s]
-            flush.zero_()                      # evict L2 between steps (outside the events)
-            ev[0].record(stream)
-            step(marks=ev)
-            ev[3].record(stream)
-            launches += 3
+            dev_step(s)
+            launches += r.launches_per_step
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
+        # the per-kernel breakdown: the three stage entry points with events between them
+        q_ms, att_ms, out_ms = r.time_stages(stage_steps, 2, flush, stream)
+        launches += r.launches_per_step * (stage_steps + 2)
         per_e2e = host_pipeline_launches(Bn, Lq, Lk, d, inp.key is not inp.query, inp.value is not inp.key)
         for s in range(Wm, Wm + K):
             e2e_step(s)
@@ -403,18 +499,19 @@ def run_gpu(args):
                 g_ev[s][0].record(stream)
                 graph.replay()
                 g_ev[s][1].record(stream)
-                launches += 3
+                launches += r.launches_per_step
             torch.cuda.synchronize()
             if world > 1:
                 dist.barrier()
+        per_wl = None
+        if rank == 0 and world == 1 and not args.no_per_workload:
+            names = [n for n in ("enc", "dec", "xattn", "tiny", "long_d128", "long") if n != args.workload]
+            per_wl, n_l = per_workload_records(names, peaks, flush, stream)
+            launches += n_l
     status = binding.mha_check_device_status(reset=True)
     if status != 0:
         raise RuntimeError(f"a pipeline wait gave up inside a kernel (status 0x{status:x})")
-    timed = evs[Wm:]
-    step_ms = [e[0].elapsed_time(e[3]) for e in timed]
-    qkv_ms = [e[0].elapsed_time(e[1]) for e in timed]
-    att_ms = [e[1].elapsed_time(e[2]) for e in timed]
-    out_ms = [e[2].elapsed_time(e[3]) for e in timed]
+    step_ms = [a.elapsed_time(b) for a, b in evs[Wm:]]
     total_ms, e2e_total = job_times(sum(step_ms), sum(a.elapsed_time(b) for a, b in e2e_ev[Wm:]), world,
                                     device="cuda")
     ms_per_step = total_ms / K
@@ -428,17 +525,11 @@ def run_gpu(args):
         g_total, _ = job_times(sum(g_ms), 0.0, world, device="cuda")
         graph_line = {"ms_per_step": g_total / K, "median_ms_per_step": statistics.median(g_ms),
                       "value": job_throughput(world, flops, g_total / K), "unit": "TFLOP/s",
-                      "note": "the step's three launches captured once in a CUDA graph, replayed; L2 flushed between replays"}
-    # attention core alone: compute rate and algorithmic bytes (Q, K, V read once, ctx written, bf16)
-    core_bytes = 2 * (Bn * Lq * d + 2 * Bn * Lk * d + Bn * Lq * d)
-    att_mean = statistics.mean(att_ms)
-    core = {"ms": att_mean, "median_ms": statistics.median(att_ms), "tflops": attn / (att_mean * 1e-3) / 1e12,
-            "algorithmic_bytes": core_bytes, "gbs": core_bytes / (att_mean * 1e-3) / 1e9,
-            "hbm_frac": core_bytes / (att_mean * 1e-3) / 1e9 / float(peaks["hbm_gbs"]),
-            "bf16_frac": attn / (att_mean * 1e-3) / 1e12 / float(peaks["bf16_tflops"])}
+                      "note": "the mha_forward call captured once in a CUDA graph, replayed; L2 flushed between replays"}
+    core = r.core_record(att_ms, peaks)
 
     # ---- roofline of the dominant kernel (largest share of the step)
-    shares = {"qkv_projection_gemm": statistics.mean(qkv_ms), "attention_core": statistics.mean(att_ms),
+    shares = {"qkv_projection_gemm": statistics.mean(q_ms), "attention_core": statistics.mean(att_ms),
               "output_projection_gemm": statistics.mean(out_ms)}
     dom = max(shares, key=shares.get)
     dom_flops = {"qkv_projection_gemm": 0.75 * proj, "attention_core": attn, "output_projection_gemm": 0.25 * proj}
@@ -453,12 +544,14 @@ def run_gpu(args):
         "dtype": "bf16", "data": "synthetic (seeded N(0,1) activations, Xavier-uniform weights)",
         "config": {"workload": DESCRIPTION[args.workload],
                    "B_per_gpu": Bn, "global_batch": Bn * world, "seq_len": Lq, "d_model": d, "h": h,
-                   "mask": ("causal" if wl.causal else "") + (" key padding" if vl is not None else ""),
+                   "mask": ("causal" if wl.causal else "") + (" key padding" if r.vl is not None else ""),
                    "parallelism": f"dp{world} (batch sharded, no collective)",
+                   "step": "one mha_forward call (the three kernels back to back)",
                    "l2": "flushed before every step (256 MB write outside the timed events)"},
         "tokens_per_s": world * Bn * Lq / (ms_per_step * 1e-3),
         "pct_of_bf16_peak": 100.0 * value / peak,
         "stage_ms": {k2: round(v2, 4) for k2, v2 in shares.items()},
+        "stage_note": f"{stage_steps} steps of the three stage entry points with CUDA events between them",
         "attention_core": core,
         "graph": graph_line,
         "roofline": {"kernel": dom, "source_sha1": source_digest(dom, args.workload), "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -466,6 +559,7 @@ def run_gpu(args):
                      "peak_source": f"{peak_src} bf16_tflops (burst); sustained {peaks.get('bf16_tflops_sustained')}"},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "api": "mha_forward_host (pinned host query in, out back)"},
+        "per_workload": per_wl,
         "gpu_launches": launches,
         "clocks": clocks,
         "cpu_baseline": cpu,
@@ -677,6 +771,8 @@ def main():
     ap.add_argument("--ref-prefix", type=int, default=2048, help="causal prefix length of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA graph replay variant")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="skip the short records of the other workloads in the JSON line")
     ap.add_argument("--decode-batch", type=int, default=16)
     ap.add_argument("--decode-context", type=int, default=8192)
     ap.add_argument("--path", choices=["mha", "ffn", "sublayer", "decode"], default="mha",
