@@ -314,6 +314,18 @@ const char* mha_last_error(void);
  */
 mha_status_t mha_check_device_status(int* status, int reset);
 
+/*
+ * Diagnostic: exercises the failure path of the bounded pipeline waits on the GPU.
+ * Enqueues on `stream` one warp that waits on an mbarrier nothing ever arrives on,
+ * through the same bounded wait every tensor-core pipeline uses but with a budget of
+ * 1024 rounds; the wait gives up, the kernel records MHA_SELFTEST_WAIT_CODE in the
+ * device status word (unless a code is already there) and ends. Read the word with
+ * mha_check_device_status. Nothing faults, traps or hangs, and no other work of the
+ * library is affected.
+ */
+#define MHA_SELFTEST_WAIT_CODE 0x7f1
+mha_status_t mha_selftest_wait_timeout(void* stream);
+
 /* Library version string. */
 const char* mha_version(void);
 

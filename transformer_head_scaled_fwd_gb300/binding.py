@@ -26,7 +26,9 @@ EXPORTS = ("mha_workspace_size", "mha_forward", "mha_qkv_projection", "mha_atten
            "mha_output_projection", "mha_host_staging_size", "mha_forward_host", "mha_last_error",
            "mha_check_device_status", "mha_version", "mha_forward_noalloc", "mha_ffn_workspace_size",
            "mha_ffn_forward", "mha_sublayer_workspace_size", "mha_sublayer_forward",
-           "mha_decode_workspace_size", "mha_kv_cache_prefill", "mha_decode_step")
+           "mha_decode_workspace_size", "mha_kv_cache_prefill", "mha_decode_step",
+           "mha_selftest_wait_timeout")
+MHA_SELFTEST_WAIT_CODE = 0x7f1
 
 
 class MHAError(RuntimeError):
@@ -91,6 +93,8 @@ def load(path: str | None = None):
         lib.mha_kv_cache_prefill.argtypes = [i] + [vp] * 5 + [i] * 4 + [vp, vp, i, vp]
         lib.mha_decode_step.restype = i
         lib.mha_decode_step.argtypes = [i] + [vp] * 9 + [i] * 3 + [vp, vp, vp, i, vp, vp, sz, vp]
+        lib.mha_selftest_wait_timeout.restype = i
+        lib.mha_selftest_wait_timeout.argtypes = [vp]
         lib.mha_forward_noalloc.restype = i
         lib.mha_forward_noalloc.argtypes = [i] + [vp] * 11 + [i] * 5 + [ctypes.POINTER(MaskT), vp, vp, vp]
         _lib = lib
@@ -258,6 +262,12 @@ def mha_ffn_forward(x, w_1, b_1, w_2, b_2, *, out, workspace, stream=None):
     _check(load().mha_ffn_forward(
         _dtype_code(x), _ptr(x), _ptr(w_1), _ptr(b_1), _ptr(w_2), _ptr(b_2), B, L, d, d_ff, _ptr(out),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def mha_selftest_wait_timeout(stream=None):
+    """Enqueue the diagnostic kernel whose bounded pipeline wait runs out (it records
+    MHA_SELFTEST_WAIT_CODE in the device status word)."""
+    _check(load().mha_selftest_wait_timeout(_stream(stream)))
 
 
 def mha_check_device_status(reset: bool = True) -> int:

@@ -120,6 +120,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
         qp = QP - 1 - r / g_heads;
         bh = grp * kHeadGroup + r % g_heads;
     }
+    MHA_DEVICE_CHECK(bh >= 0 && bh < BH && qp >= 0 && qp < QP && p.Lq >= 1 && p.Lk >= 1 &&
+                         QP * 2 * kAttnBM >= p.Lq,
+                     p.status, 0x2f0);
     const int b = bh / p.h;
     const int head = bh - b * p.h;
     const int q0 = qp * 2 * kAttnBM;

@@ -75,6 +75,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_d128_kernel(const __grid_con
     const int r = idx - grp * kHeadGroup * QT;
     const int qt = QT - 1 - r / g_heads;
     const int bh = grp * kHeadGroup + r % g_heads;
+    MHA_DEVICE_CHECK(bh >= 0 && bh < BH && qt >= 0 && qt < QT && p.Lq >= 1 && p.Lk >= 1 && QT * BM >= p.Lq,
+                     p.status, 0x2f1);
     const int b = bh / p.h;
     const int head = bh - b * p.h;
     const int q0 = qt * BM;

@@ -83,6 +83,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
     const int n_tiles = (p.N + BN - 1) / BN;
     int total = 0;
     for (int g = 0; g < p.ngroups; ++g) total += p.g[g].m_tiles * n_tiles;
+    MHA_DEVICE_CHECK(gemm_params_ok(p), p.status, 0x1f0);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kGemmStages; ++s) {

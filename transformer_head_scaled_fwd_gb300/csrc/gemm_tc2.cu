@@ -126,6 +126,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     const int n_tiles = (p.N + BN - 1) / BN;
     const int total = pair_units(p, n_tiles);
     const bool shared_rows = groups_share_rows(p);
+    MHA_DEVICE_CHECK(gemm_params_ok(p), p.status, 0x1f1);   // uniform: both CTAs of a pair return
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {

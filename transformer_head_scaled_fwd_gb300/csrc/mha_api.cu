@@ -1115,6 +1115,14 @@ mha_status_t mha_forward_host(mha_dtype_t dt, const void* h_query, const void* h
     return MHA_OK;
 }
 
+mha_status_t mha_selftest_wait_timeout(void* stream) {
+    int* st = device_status_ptr();
+    if (!st) return fail(MHA_ERR_CUDA, "device status word unavailable");
+    cudaError_t e = mha::launch_wait_timeout_selftest(st, MHA_SELFTEST_WAIT_CODE, as_stream(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "wait-timeout self-test launch");
+    return MHA_OK;
+}
+
 mha_status_t mha_check_device_status(int* status, int reset) {
     if (!status) return fail(MHA_ERR_INVALID_ARG, "status must not be NULL");
     cudaError_t e = cudaDeviceSynchronize();

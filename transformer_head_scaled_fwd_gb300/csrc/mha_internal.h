@@ -47,6 +47,19 @@ struct GemmParams {
     int* status;
 };
 
+// The tile bookkeeping of a GemmParams is consistent: 1 to 3 groups, K a positive
+// multiple of 64, N positive, and every group's tiles cover its rows exactly.
+__host__ __device__ inline bool gemm_params_ok(const GemmParams& p) {
+    if (p.ngroups < 1 || p.ngroups > 3 || p.K <= 0 || p.K % kGemmBK != 0 || p.N <= 0) return false;
+    for (int g = 0; g < p.ngroups; ++g) {
+        const GemmGroup& G = p.g[g];
+        if (G.L <= 0 || G.tiles_per_b != (G.L + kGemmBM - 1) / kGemmBM || G.m_tiles <= 0 ||
+            G.m_tiles % G.tiles_per_b != 0)
+            return false;
+    }
+    return p.out_plain != 0 || p.dk_slabs >= 1;
+}
+
 size_t gemm_tc_smem_bytes();
 cudaError_t launch_gemm_tc(const GemmParams& p, int max_m_tiles, cudaStream_t s);
 
@@ -92,6 +105,11 @@ struct PattnParams {
     float scale_log2;
 };
 cudaError_t launch_pattn_bf16(const PattnParams& p, cudaStream_t s);
+
+// ------------------------------------------------------------ diagnostics
+// One warp waits on an mbarrier nothing arrives on, through the bounded pipeline wait
+// with a small budget; on giving up it records `code` in *status (selftest.cu).
+cudaError_t launch_wait_timeout_selftest(int* status, int code, cudaStream_t s);
 
 // ------------------------------------------------------------ fp32 SIMT path
 struct F32GemmGroup {

@@ -45,15 +45,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // broken pipeline ends the kernel instead of hanging the GPU.
 constexpr uint32_t kWaitLimit = 1u << 24;
 
-// Bounded wait on phase `parity` of `bar`. On giving up it records `code` in
-// *status, raises the CTA-wide abort flag and returns false; once the abort
-// flag is up, every later wait of the CTA returns at once, so the kernel runs
-// to its end (freeing its tensor memory) with invalid results.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status, int code) {
+// Bounded wait on phase `parity` of `bar`, at most kLimit try_wait rounds. On giving
+// up it records `code` in *status, raises the CTA-wide abort flag and returns false;
+// once the abort flag is up, every later wait of the CTA returns at once, so the
+// kernel runs to its end (freeing its tensor memory) with invalid results.
+template <uint32_t kLimit>
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                int* status, int code) {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
-    for (uint32_t it = 1; it < kWaitLimit; ++it) {
+    for (uint32_t it = 1; it < kLimit; ++it) {
         if (mbar_try_wait(a, parity)) return true;
         if ((it & 255u) == 0 && *abort_flag) return false;
     }
@@ -61,6 +62,29 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     atomicCAS(status, 0, code);
     return false;
 }
+// The pipeline waits of every kernel: the bounded wait with the library's budget.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          int* status, int code) {
+    return mbar_wait_limit<kWaitLimit>(bar, parity, abort_flag, status, code);
+}
+
+// Debug builds (compiled with MHA_DEVICE_CHECKS) check a kernel's own indices at
+// its entry, before any barrier, tensor-memory allocation or copy: a CTA whose
+// block or tile index falls outside the problem records `code` in *status and
+// returns without touching memory. Release builds compile the check away.
+#ifdef MHA_DEVICE_CHECKS
+#define MHA_DEVICE_CHECK(cond, status, code)          \
+    do {                                               \
+        if (!(cond)) {                                 \
+            if (threadIdx.x == 0) atomicCAS((status), 0, (code)); \
+            return;                                    \
+        }                                              \
+    } while (0)
+#else
+#define MHA_DEVICE_CHECK(cond, status, code) \
+    do {                                     \
+    } while (0)
+#endif
 
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
