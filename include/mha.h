@@ -36,9 +36,11 @@
  *   - dt selects the storage type of query/key/value/weights/biases/out and of
  *     the workspace tensors: MHA_F32 (fp32 everywhere, fp32 SIMT arithmetic,
  *     any d_k <= 256) or MHA_BF16 (bf16 storage, fp32 accumulation on the
- *     tensor cores, d_k = 64 or 128; mha_forward and mha_forward_noalloc also
- *     take any other d_k <= 256 in bf16, which they run on the fp32 kernels over
- *     fp32 copies held in the workspace, then round the output to bf16).
+ *     tensor cores, d_k = 64 or 128, or d_k = 8, 16, 32 when d_model is a
+ *     multiple of 64 (those heads run on the d_k = 64 kernels, zero-padded to 64
+ *     columns on load); mha_forward and mha_forward_noalloc also take any other
+ *     d_k <= 256 in bf16, which they run on the fp32 kernels over fp32 copies held
+ *     in the workspace, then round the output to bf16).
  *     p_attn is always fp32.
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and the call returns without waiting for it.
@@ -83,9 +85,9 @@ typedef struct {
  *   KVh  [B, 2, h, L_k, d_k]   head-split projected keys (slot 0) and values (slot 1)
  *   ctx  [B, L_q, d_model]     concatenated head outputs (input of W_o)
  *   stat [B, h, L_q, 2] fp32   per-row softmax statistics (max, sum) used for p_attn
- * For MHA_BF16 with d_k other than 64 and 128 (d_k <= 256): the MHA_F32 workspace of
- * the same sizes, then fp32 copies of query, key, value [B, L, d_model], of the four
- * weights and biases and of out, each 256-byte aligned.
+ * For MHA_BF16 with a d_k the tensor-core kernels do not take (d_k <= 256): the MHA_F32
+ * workspace of the same sizes, then fp32 copies of query, key, value [B, L, d_model], of
+ * the four weights and biases and of out, each 256-byte aligned.
  * Returns 0 for invalid sizes.
  */
 size_t mha_workspace_size(mha_dtype_t dt, int B, int L_q, int L_k, int d_model, int h);

@@ -491,16 +491,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
             uint32_t o[64];
             tmem_ld_x64(o_tmem, o);
             const float inv = 1.0f / l;
-            // Q_t's tile is free (its last S MMA completed before the last softmax): stage there.
-            const uint32_t stage = smem_u32(base + kOffQ + t * kTileBytes) + row * 128;
+            // Q_t's tile is free (its last S MMA completed before the last softmax): stage there,
+            // 128-byte swizzled rows of 64 columns, or for heads narrower than 64 a dense tile of
+            // their d_k columns (the rest of O is the zero padding's).
+            const int nd = p.narrow_dk;
+            const uint32_t stage = smem_u32(base + kOffQ + t * kTileBytes) + row * (nd ? nd * 2 : 128);
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch) {
+                if (nd && ch * 8 >= nd) break;
                 uint32_t w[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     w[e] = pack_bf16x2(__uint_as_float(o[ch * 8 + 2 * e]) * inv,
                                        __uint_as_float(o[ch * 8 + 2 * e + 1]) * inv);
-                st_shared_v4(stage + ((ch ^ (row & 7)) << 4), w[0], w[1], w[2], w[3]);
+                st_shared_v4(stage + ((nd ? ch : (ch ^ (row & 7))) << 4), w[0], w[1], w[2], w[3]);
             }
             if (p.stats != nullptr && qi < p.Lq) {
                 float2* st = reinterpret_cast<float2*>(p.stats) + (static_cast<long>(tq_slab) * p.Lq + qi);
@@ -509,7 +513,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
             fence_proxy_async_smem();
             named_bar_sync(1 + t, kAttnBM);
             if (row == 0 && !*abort_flag) {
-                tma_store_3d(&p.ctx_map, base + kOffQ + t * kTileBytes, thead * kAttnD, qt0, tb);
+                tma_store_3d(&p.ctx_map, base + kOffQ + t * kTileBytes, thead * (nd ? nd : kAttnD), qt0, tb);
                 tma_store_commit();
                 tma_store_wait_all();
             }
@@ -597,10 +601,13 @@ cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t s) {
 
 cudaError_t launch_pattn_bf16(const PattnParams& p, cudaStream_t s) {
     dim3 grid((p.Lq + kPRows - 1) / kPRows, p.B * p.h);
-    if (p.dk == 128)
-        pattn_bf16_kernel<128><<<grid, kPKeys, 0, s>>>(p);
-    else
-        pattn_bf16_kernel<64><<<grid, kPKeys, 0, s>>>(p);
+    switch (p.dk) {
+        case 128: pattn_bf16_kernel<128><<<grid, kPKeys, 0, s>>>(p); break;
+        case 32: pattn_bf16_kernel<32><<<grid, kPKeys, 0, s>>>(p); break;
+        case 16: pattn_bf16_kernel<16><<<grid, kPKeys, 0, s>>>(p); break;
+        case 8: pattn_bf16_kernel<8><<<grid, kPKeys, 0, s>>>(p); break;
+        default: pattn_bf16_kernel<64><<<grid, kPKeys, 0, s>>>(p); break;
+    }
     return cudaGetLastError();
 }
 

@@ -269,7 +269,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                 // the TMA store that last used this staging buffer must have read it
                 if (issuer && slabs_issued >= 2) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
                 named_bar_sync(1, 128);
-                const uint32_t stage = smem_u32(base + kOffStage + sb * kSlabBytes) + row * 128;
+                const uint32_t sbuf = smem_u32(base + kOffStage + sb * kSlabBytes);
+                const uint32_t stage = sbuf + row * 128;
+                const int nsh = p.narrow_shift;   // heads narrower than 64: log2(d_k), else 0
                 const bool has_res = G.residual != nullptr && c.l0 + row < G.L;
                 const __nv_bfloat16* res_row =
                     has_res ? G.residual + (static_cast<long>(c.b) * G.L + c.l0 + row) * p.N + n : nullptr;
@@ -297,7 +299,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                         }
                         w[e] = pack_bf16x2(y0, y1);
                     }
-                    st_shared_v4(stage + ((ch ^ (row & 7)) << 4), w[0], w[1], w[2], w[3]);
+                    // 128-byte swizzled rows, or (narrow heads) dense head-major sub-tiles:
+                    // head (8 ch) / d_k at ((head * 128 + row) * d_k + (8 ch) % d_k) * 2
+                    const uint32_t dst = nsh ? sbuf + ((((ch * 8) >> nsh) * 128 + row) << (nsh + 1)) +
+                                                   (((ch * 8) & ((1 << nsh) - 1)) << 1)
+                                             : stage + ((ch ^ (row & 7)) << 4);
+                    st_shared_v4(dst, w[0], w[1], w[2], w[3]);
                 }
                 fence_proxy_async_smem();
                 named_bar_sync(1, 128);
@@ -305,6 +312,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                     const uint8_t* src = base + kOffStage + sb * kSlabBytes;
                     if (p.out_plain)
                         tma_store_3d(&p.out[c.grp], src, n, c.l0, c.b);
+                    else if (nsh)   // the slab's 64 >> nsh heads, planes from out_j0 + (n/64) * (64 >> nsh)
+                        tma_store_4d(&p.out[c.grp], src, 0, c.l0, G.out_j0 + (n / 64) * (64 >> nsh), c.b);
                     else   // slab n/64 of the group: head (n/64) / dk_slabs, half (n/64) % dk_slabs
                         tma_store_5d(&p.out[c.grp], src, 0, (n / 64) % p.dk_slabs, c.l0,
                                      G.out_j0 + (n / 64) / p.dk_slabs, c.b);

@@ -97,12 +97,14 @@ mha_status_t get_encoder() {
     return MHA_OK;
 }
 
-// bf16 tiled map, 128-byte swizzle, zero fill out of bounds.
+// bf16 tiled map, 128-byte swizzle (or none), zero fill out of bounds.
 mha_status_t encode_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
-                         const uint64_t* strides_bytes, const uint32_t* box, const char* what) {
+                         const uint64_t* strides_bytes, const uint32_t* box, const char* what,
+                         bool swizzle = true) {
     uint32_t estr[5] = {1, 1, 1, 1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides_bytes,
-                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(MHA_ERR_CUDA, "tensor map encode failed for %s (CUresult %d)", what, (int)r);
     return MHA_OK;
@@ -170,6 +172,28 @@ mha_status_t map_heads4d(CUtensorMap* m, const void* base, int planes, int L, in
     const uint32_t box[4] = {64, 1, 128, 1};
     return encode_bf16(m, base, 4, dims, str, box, "head-split input");
 }
+// Heads narrower than 64 (d_k = 8, 16, 32: 64 / d_k heads per 64-column slab of a
+// projection tile). Projection store: head-split [B, planes, L_stride, d_k] as
+// {d_k, L, planes, B}, unswizzled; a box {d_k, 128, 64/d_k, 1} holds the slab's heads
+// one after the other (the GEMM epilogue stages them head-major, each 128 x d_k dense).
+mha_status_t map_heads4_narrow(CUtensorMap* m, const void* base, int B, int planes, int L, int dk,
+                               int L_stride = 0) {
+    if (L_stride <= 0) L_stride = L;
+    const uint64_t plane = (uint64_t)L_stride * dk * 2;
+    const uint64_t dims[4] = {(uint64_t)dk, (uint64_t)L, (uint64_t)planes, (uint64_t)B};
+    const uint64_t str[3] = {(uint64_t)dk * 2, plane, (uint64_t)planes * plane};
+    const uint32_t box[4] = {(uint32_t)dk, 128, (uint32_t)(64 / dk), 1};
+    return encode_bf16(m, base, 4, dims, str, box, "narrow head-split output", false);
+}
+// Attention loads of narrow heads: [planes, L, d_k] as {d_k, L, planes} with a box of 64
+// columns: the columns past d_k are out of bounds and arrive as zeros, so the d_k = 64
+// kernel computes exactly the narrow head's scores and a zero-padded P.V.
+mha_status_t map_heads3_narrow(CUtensorMap* m, const void* base, int planes, int L, int dk) {
+    const uint64_t dims[3] = {(uint64_t)dk, (uint64_t)L, (uint64_t)planes};
+    const uint64_t str[2] = {(uint64_t)dk * 2, (uint64_t)L * dk * 2};
+    const uint32_t box[3] = {64, 128, 1};
+    return encode_bf16(m, base, 3, dims, str, box, "narrow head-split input");
+}
 // head-split [planes, L, 64] as {64, L, planes}, box {64, 128, 1}
 mha_status_t map_heads3(CUtensorMap* m, const void* base, int planes, int L) {
     const uint64_t dims[3] = {64, (uint64_t)L, (uint64_t)planes};
@@ -187,9 +211,14 @@ int* device_status_ptr() {
 // ---------------------------------------------------------------- validation
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Heads narrower than 64 that the d_k = 64 kernels take (zero-padded to 64 columns).
+bool narrow_dk(int d, int h) {
+    const int dk = d / h;
+    return (dk == 8 || dk == 16 || dk == 32) && d % 64 == 0;
+}
 // bf16 head widths the tensor-core kernels take; other widths up to 256 run (in
 // mha_forward only) on the fp32 kernels over converted copies.
-bool bf16_native_dk(int dk) { return dk == 64 || dk == 128; }
+bool bf16_native(int d, int h) { return d / h == 64 || d / h == 128 || narrow_dk(d, h); }
 
 mha_status_t check_sizes(mha_dtype_t dt, int B, int Lq, int Lk, int d, int h, bool bf16_any_dk = false) {
     if (dt != MHA_F32 && dt != MHA_BF16) return fail(MHA_ERR_INVALID_ARG, "dtype %d is not MHA_F32 or MHA_BF16", dt);
@@ -198,8 +227,10 @@ mha_status_t check_sizes(mha_dtype_t dt, int B, int Lq, int Lk, int d, int h, bo
                     h);
     if (d % h != 0) return fail(MHA_ERR_INVALID_ARG, "d_model %% h != 0 (d_model=%d, h=%d)", d, h);
     const int dk = d / h;
-    if (dt == MHA_BF16 && !bf16_native_dk(dk) && !(bf16_any_dk && dk <= 256))
-        return fail(MHA_ERR_UNSUPPORTED, "this bf16 entry point implements d_k = 64 and 128 (d_k = %d)", dk);
+    if (dt == MHA_BF16 && !bf16_native(d, h) && !(bf16_any_dk && dk <= 256))
+        return fail(MHA_ERR_UNSUPPORTED,
+                    "this bf16 entry point implements d_k = 64 and 128, and 8, 16, 32 with d_model %% 64 == 0 "
+                    "(d_k = %d, d_model = %d)", dk, d);
     if (dk > 256) return fail(MHA_ERR_UNSUPPORTED, "d_k <= 256 is implemented (d_k = %d)", dk);
     const double big = static_cast<double>(B) * h * Lq * Lk;
     if (static_cast<double>(B) * Lq * d > 4.0e9 || static_cast<double>(B) * Lk * d * 2 > 4.0e9 || big > 1.0e15)
@@ -261,7 +292,7 @@ const char* mha_last_error(void) { return g_last_error.c_str(); }
 size_t mha_workspace_size(mha_dtype_t dt, int B, int L_q, int L_k, int d_model, int h) {
     Layout L;
     if (!layout_of(dt, B, L_q, L_k, d_model, h, &L)) return 0;
-    if (dt == MHA_BF16 && !bf16_native_dk(d_model / h) && d_model / h <= 256) {
+    if (dt == MHA_BF16 && !bf16_native(d_model, h) && d_model / h <= 256) {
         F32Copies C;
         f32_copies_of(B, L_q, L_k, d_model, h, &C);
         return C.total;
@@ -342,6 +373,7 @@ mha_status_t qkv_bf16_impl(const void* query, const void* key, const void* value
                            int L_k, int d_model, int h, const Layout& L, uint8_t* ws, cudaStream_t s, int r0,
                            int rows) {
     const int dk = d_model / h;
+    const bool narrow = narrow_dk(d_model, h);
     mha_status_t st;
     if ((st = get_encoder()) != MHA_OK) return st;
     mha::GemmParams p;
@@ -358,7 +390,11 @@ mha_status_t qkv_bf16_impl(const void* query, const void* key, const void* value
         if ((st = map_rows(&p.a[g], static_cast<const uint8_t*>(A[g]) + in_off, B, Ls[g], d_model,
                            "projection input", Lfull[g])) != MHA_OK)
             return st;
-        if (g == 0) {
+        if (narrow) {
+            st = (g == 0) ? map_heads4_narrow(&p.out[g], ws + L.q + out_off, B, h, Ls[g], dk, L_q)
+                          : map_heads4_narrow(&p.out[g], ws + L.kv + out_off, B, 2 * h, Ls[g], dk, L_k);
+            if (st != MHA_OK) return st;
+        } else if (g == 0) {
             if ((st = map_heads5(&p.out[g], ws + L.q + out_off, B, h, Ls[g], dk / 64, L_q)) != MHA_OK) return st;
         } else {
             if ((st = map_heads5(&p.out[g], ws + L.kv + out_off, B, 2 * h, Ls[g], dk / 64, L_k)) != MHA_OK)
@@ -367,7 +403,7 @@ mha_status_t qkv_bf16_impl(const void* query, const void* key, const void* value
         p.g[g].L = Ls[g];
         p.g[g].tiles_per_b = (Ls[g] + mha::kGemmBM - 1) / mha::kGemmBM;
         p.g[g].m_tiles = B * p.g[g].tiles_per_b;
-        p.g[g].out_j0 = (g == 2) ? h : 0;
+        p.g[g].out_j0 = (g == 2) ? h : 0;   // first plane of V in KVh
         p.g[g].bias = static_cast<const __nv_bfloat16*>(bias[g]);
         max_m = std::max(max_m, p.g[g].m_tiles);
     }
@@ -375,7 +411,8 @@ mha_status_t qkv_bf16_impl(const void* query, const void* key, const void* value
     p.K = d_model;
     p.N = d_model;
     p.out_plain = 0;
-    p.dk_slabs = dk / 64;
+    p.dk_slabs = narrow ? 1 : dk / 64;
+    p.narrow_shift = narrow ? (dk == 8 ? 3 : dk == 16 ? 4 : 5) : 0;
     p.status = device_status_ptr();
     if (!p.status) return fail(MHA_ERR_CUDA, "device status word unavailable");
     (void)max_m;
@@ -427,23 +464,38 @@ mha_status_t attention_impl(mha_dtype_t dt, int B, int L_q, int L_k, int d_model
     if ((st = get_encoder()) != MHA_OK) return st;
     mha::AttnParams p;
     memset(&p, 0, sizeof(p));
+    const bool narrow = narrow_dk(d_model, h);
     if (dk == 64) {
         if ((st = map_heads3(&p.q_map, ws + L.q, B * h, L_q)) != MHA_OK) return st;
         if ((st = map_heads3(&p.kv_map, ws + L.kv, B * 2 * h, L_k)) != MHA_OK) return st;
+    } else if (narrow) {
+        if ((st = map_heads3_narrow(&p.q_map, ws + L.q, B * h, L_q, dk)) != MHA_OK) return st;
+        if ((st = map_heads3_narrow(&p.kv_map, ws + L.kv, B * 2 * h, L_k, dk)) != MHA_OK) return st;
     } else {
         if ((st = map_heads4d(&p.q_map, ws + L.q, B * h, L_q, dk / 64)) != MHA_OK) return st;
         if ((st = map_heads4d(&p.kv_map, ws + L.kv, B * 2 * h, L_k, dk / 64)) != MHA_OK) return st;
     }
-    if ((st = map_rows(&p.ctx_map, ws + L.ctx, B, L_q, d_model, "context")) != MHA_OK) return st;
+    if (narrow) {
+        // the head's d_k columns of ctx, stored from a dense (unswizzled) 128 x d_k staging tile
+        const uint64_t dims[3] = {(uint64_t)d_model, (uint64_t)L_q, (uint64_t)B};
+        const uint64_t str[2] = {(uint64_t)d_model * 2, (uint64_t)L_q * d_model * 2};
+        const uint32_t box[3] = {(uint32_t)dk, 128, 1};
+        if ((st = encode_bf16(&p.ctx_map, ws + L.ctx, 3, dims, str, box, "context (narrow heads)", false)) != MHA_OK)
+            return st;
+        p.narrow_dk = dk;
+    } else if ((st = map_rows(&p.ctx_map, ws + L.ctx, B, L_q, d_model, "context")) != MHA_OK) {
+        return st;
+    }
     p.B = B; p.h = h; p.Lq = L_q; p.Lk = L_k;
     p.causal = causal; p.valid_lens = vl; p.dense = dense; p.dense_mq = dmq;
     p.stats = p_attn ? reinterpret_cast<float*>(ws + L.stat) : nullptr;
     p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(dk)));
-    const int q_rows = dk == 64 ? 2 * mha::kAttnBM : mha::kAttnBM;   // query rows per CTA
+    const bool d128 = dk == 128;
+    const int q_rows = d128 ? mha::kAttnBM : 2 * mha::kAttnBM;   // query rows per CTA
     p.q_pairs = (L_q + q_rows - 1) / q_rows;
     p.status = device_status_ptr();
     if (!p.status) return fail(MHA_ERR_CUDA, "device status word unavailable");
-    cudaError_t e = dk == 64 ? mha::launch_attn_tc(p, s) : mha::launch_attn_tc_d128(p, s);
+    cudaError_t e = d128 ? mha::launch_attn_tc_d128(p, s) : mha::launch_attn_tc(p, s);
     if (e != cudaSuccess) return cuda_fail(e, "attention launch");
     if (p_attn) {
         mha::PattnParams pp{};
@@ -588,7 +640,7 @@ mha_status_t mha_forward(mha_dtype_t dt, const void* query, const void* key, con
     if ((st = check_mask(mask, L_q, L_k)) != MHA_OK) return st;
     if (!query || !key || !value || !w_q || !w_k || !w_v || !w_o || !out)
         return fail(MHA_ERR_INVALID_ARG, "query, key, value, W_q, W_k, W_v, W_o and out must not be NULL");
-    if (dt == MHA_BF16 && !bf16_native_dk(d_model / h))
+    if (dt == MHA_BF16 && !bf16_native(d_model, h))
         return forward_bf16_on_f32(query, key, value, w_q, b_q, w_k, b_k, w_v, b_v, w_o, b_o, B, L_q, L_k, d_model,
                                    h, mask, out, p_attn, workspace, workspace_bytes, as_stream(stream));
     Layout L;

@@ -43,6 +43,8 @@ struct GemmParams {
     int N;
     int out_plain;        // 1: plain [B, L, N] output
     int dk_slabs;         // head-split output: d_k / 64 (64-column slabs per head)
+    int narrow_shift;     // head-split output of heads narrower than 64: log2(d_k) (3, 4, 5), else 0;
+                          // out map {d_k, L, planes, B}, box {d_k, 128, 64/d_k, 1}, unswizzled
     int relu;             // 1: max(0, .) after the bias (first FFN layer)
     int* status;
 };
@@ -82,6 +84,8 @@ struct AttnParams {
     float* stats;          // [B, h, L_q, 2] (max in log2 units, sum) or nullptr
     float scale_log2;      // log2(e) / sqrt(d_k)
     int q_pairs;           // ceil(L_q / 256)
+    int narrow_dk;         // d_k of heads narrower than 64 (8, 16, 32: q_map / kv_map zero-pad
+                           // them to 64 columns, ctx_map stores d_k columns unswizzled); 0 otherwise
     int* status;
 };
 
