@@ -570,6 +570,66 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+def run_gpu_pattn(args):
+    """The optional attention weights (p_attn, fp32 [B, h, L_q, L_k]): the attention stage timed
+    with and without them on the same workload. The difference is the p_attn pass (the scores
+    recomputed from Qh, Kh and the row statistics, normalised and written); HBM-write bound, so
+    it is reported as GB/s of the fp32 weights written against the measured copy bandwidth."""
+    import torch
+
+    from transformer_head_scaled_fwd_gb300 import binding
+    from transformer_head_scaled_fwd_gb300 import build as B
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    B.build()
+    binding.load()
+    peaks, peak_src = load_peaks()
+    r = WorkloadRun(args.workload, rank, local)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    p_attn = torch.empty(r.B, r.h, r.Lq, r.Lk, dtype=torch.float32, device="cuda")
+    K, Wm = args.steps, args.warmup
+    binding.mha_qkv_projection(r.q, r.k, r.v, r.Wt["w_q"], r.Wt["b_q"], r.Wt["w_k"], r.Wt["b_k"], r.Wt["w_v"],
+                               r.Wt["b_v"], r.h, workspace=r.ws, stream=stream)
+
+    def attn_ms(with_p):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K + Wm)]
+        for s_ in range(Wm + K):
+            flush.zero_()
+            ev[s_][0].record(stream)
+            binding.mha_attention_core(r.dt, r.B, r.Lq, r.Lk, r.d, r.h, workspace=r.ws, mask=r.mask,
+                                       p_attn=p_attn if with_p else None, stream=stream)
+            ev[s_][1].record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in ev[Wm:]]
+
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        without = attn_ms(False)
+        with_p = attn_ms(True)
+    if binding.mha_check_device_status(reset=True) != 0:
+        raise RuntimeError("a pipeline wait gave up inside a kernel")
+    rows = p_attn.sum(-1)
+    rowsum_err = float((rows - 1.0).abs().max().item())
+    ms = statistics.mean(with_p) - statistics.mean(without)
+    nbytes = p_attn.numel() * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peak = float(peaks["hbm_gbs"])
+    line = {
+        "metric": "MHA p_attn pass GB/s (fp32 weights written)", "value": gbs, "unit": "GB/s", "n_gpus": 1,
+        "steps": K, "warmup": Wm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded)",
+        "config": {"workload": DESCRIPTION[args.workload] + ", with p_attn", "l2": "flushed before every step"},
+        "attention_ms": {"without_p_attn": statistics.mean(without), "with_p_attn": statistics.mean(with_p)},
+        "p_attn_bytes": nbytes, "p_attn_row_sum_max_err": rowsum_err,
+        "roofline": {"kernel": "pattn_bf16_kernel", "bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                     "frac": gbs / peak, "traffic": None, "peak_source": f"{peak_src} hbm_gbs"},
+        "gpu_launches": 3 * (K + Wm) + 2, "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_gpu_ffn(args):
     """Position-wise FFN (max(0, x W_1 + b_1) W_2 + b_2) on one GPU: TFLOP/s of the two GEMMs."""
     import torch
@@ -775,9 +835,10 @@ def main():
                     help="skip the short records of the other workloads in the JSON line")
     ap.add_argument("--decode-batch", type=int, default=16)
     ap.add_argument("--decode-context", type=int, default=8192)
-    ap.add_argument("--path", choices=["mha", "ffn", "sublayer", "decode"], default="mha",
+    ap.add_argument("--path", choices=["mha", "ffn", "sublayer", "decode", "pattn"], default="mha",
                     help="mha: the attention sublayer (default); ffn: the position-wise FFN; "
-                         "sublayer: x + MHA(LayerNorm(x)); decode: one token per sequence vs a KV cache")
+                         "sublayer: x + MHA(LayerNorm(x)); decode: one token per sequence vs a KV cache; "
+                         "pattn: the attention stage with and without the p_attn weights")
     ap.add_argument("--ffn-workload", default="ffn_long", choices=["ffn_base", "ffn_long"])
     args = ap.parse_args()
     if args.warmup < 3 and args.impl != "reference":
@@ -790,6 +851,8 @@ def main():
         run_gpu_sublayer(args)
     elif args.path == "decode":
         run_gpu_decode(args)
+    elif args.path == "pattn":
+        run_gpu_pattn(args)
     else:
         run_gpu(args)
 

@@ -523,65 +523,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
     }
 }
 
-// ------------------------------------------------------------------ p_attn (bf16 path)
-// p_attn[b, h, i, j] = exp2(u_ij - m_i) / l_i with the row statistics written by
-// the attention kernel; u_ij recomputed from the bf16 Qh, Kh in fp32.
-constexpr int kPRows = 32;     // query rows per block
-constexpr int kPKeys = 128;    // keys per pass (one per thread)
-
-template <int D>
-__global__ void __launch_bounds__(kPKeys) pattn_bf16_kernel(const PattnParams p) {
-    __shared__ float qs[kPRows][D];
-    __shared__ float2 st[kPRows];
-    const int bh = blockIdx.y;
-    const int b = bh / p.h;
-    const int head = bh - b * p.h;
-    const int i0 = blockIdx.x * kPRows;
-    const __nv_bfloat16* q = p.q + (static_cast<long>(bh) * p.Lq) * D;
-    const __nv_bfloat16* k = p.kv + (static_cast<long>(b) * 2 * p.h + head) * p.Lk * D;
-    for (int e = threadIdx.x; e < kPRows * D; e += blockDim.x) {
-        const int r = e / D, c = e % D;
-        qs[r][c] = (i0 + r < p.Lq) ? __bfloat162float(q[static_cast<long>(i0 + r) * D + c]) : 0.0f;
-    }
-    for (int r = threadIdx.x; r < kPRows; r += blockDim.x)
-        st[r] = (i0 + r < p.Lq) ? reinterpret_cast<const float2*>(p.stats)[static_cast<long>(bh) * p.Lq + i0 + r]
-                                : make_float2(0.f, 1.f);
-    __syncthreads();
-    int vl = p.Lk;
-    if (p.valid_lens != nullptr) vl = min(max(p.valid_lens[b], 0), p.Lk);
-    for (int k0 = 0; k0 < p.Lk; k0 += kPKeys) {
-        const int kj = k0 + threadIdx.x;
-        if (kj >= p.Lk) continue;
-        float kr[D];
-#pragma unroll
-        for (int c = 0; c < D; c += 8) {
-            const uint4 raw = *reinterpret_cast<const uint4*>(k + static_cast<long>(kj) * D + c);
-            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 f = __bfloat1622float2(h2[e]);
-                kr[c + 2 * e] = f.x;
-                kr[c + 2 * e + 1] = f.y;
-            }
-        }
-        for (int r = 0; r < kPRows; ++r) {
-            const int qi = i0 + r;
-            if (qi >= p.Lq) break;
-            float dot = 0.f;
-#pragma unroll
-            for (int c = 0; c < D; ++c) dot = fmaf(qs[r][c], kr[c], dot);
-            bool ok = !(p.causal && kj > qi) && kj < vl;
-            if (ok && p.dense != nullptr) {
-                const long mrow = (p.dense_mq == 1) ? 0 : qi;
-                const long mq = (p.dense_mq == 1) ? 1 : p.Lq;
-                ok = p.dense[(static_cast<long>(b) * mq + mrow) * p.Lk + kj] != 0;
-            }
-            const float u = ok ? dot * p.scale_log2 : kMaskedLog2;
-            p.p_attn[(static_cast<long>(bh) * p.Lq + qi) * p.Lk + kj] = ex2_approx(u - st[r].x) / st[r].y;
-        }
-    }
-}
-
 }  // namespace
 
 size_t attn_tc_smem_bytes() { return kSmemBytes; }
@@ -597,18 +538,6 @@ cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     const unsigned grid = two ? static_cast<unsigned>((BH + 1) / 2) : static_cast<unsigned>(p.q_pairs) * p.B * p.h;
     return launch_pdl(kern, dim3(grid), dim3(kAttnThreads), kSmemBytes, s, p);
-}
-
-cudaError_t launch_pattn_bf16(const PattnParams& p, cudaStream_t s) {
-    dim3 grid((p.Lq + kPRows - 1) / kPRows, p.B * p.h);
-    switch (p.dk) {
-        case 128: pattn_bf16_kernel<128><<<grid, kPKeys, 0, s>>>(p); break;
-        case 32: pattn_bf16_kernel<32><<<grid, kPKeys, 0, s>>>(p); break;
-        case 16: pattn_bf16_kernel<16><<<grid, kPKeys, 0, s>>>(p); break;
-        case 8: pattn_bf16_kernel<8><<<grid, kPKeys, 0, s>>>(p); break;
-        default: pattn_bf16_kernel<64><<<grid, kPKeys, 0, s>>>(p); break;
-    }
-    return cudaGetLastError();
 }
 
 }  // namespace mha

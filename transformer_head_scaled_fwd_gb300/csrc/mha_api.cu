@@ -498,16 +498,19 @@ mha_status_t attention_impl(mha_dtype_t dt, int B, int L_q, int L_k, int d_model
     cudaError_t e = d128 ? mha::launch_attn_tc_d128(p, s) : mha::launch_attn_tc(p, s);
     if (e != cudaSuccess) return cuda_fail(e, "attention launch");
     if (p_attn) {
-        mha::PattnParams pp{};
-        pp.q = reinterpret_cast<const __nv_bfloat16*>(ws + L.q);
-        pp.kv = reinterpret_cast<const __nv_bfloat16*>(ws + L.kv);
-        pp.stats = p.stats;
-        pp.p_attn = p_attn;
-        pp.B = B; pp.h = h; pp.Lq = L_q; pp.Lk = L_k;
-        pp.causal = causal; pp.valid_lens = vl; pp.dense = dense; pp.dense_mq = dmq;
-        pp.scale_log2 = p.scale_log2;
-        pp.dk = dk;
-        e = mha::launch_pattn_bf16(pp, s);
+        p.p_attn = p_attn;
+        if (L_k % 4 == 0 && aligned16(p_attn)) {
+            // fp32 [B*h, L_q, L_k] as {L_k, L_q, B*h}, box {32, 128, 1}, 128-byte swizzle
+            const uint64_t dims[3] = {(uint64_t)L_k, (uint64_t)L_q, (uint64_t)B * h};
+            const uint64_t str[2] = {(uint64_t)L_k * 4, (uint64_t)L_q * L_k * 4};
+            const uint32_t box[3] = {32, 128, 1};
+            uint32_t estr[3] = {1, 1, 1};
+            CUresult r = g_encode(&p.p_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p_attn, dims, str, box, estr,
+                                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (r != CUDA_SUCCESS) return fail(MHA_ERR_CUDA, "tensor map encode failed for p_attn (CUresult %d)", (int)r);
+        }
+        e = mha::launch_pattn_tc(p, d128 ? 2 : 1, s);
         if (e != cudaSuccess) return cuda_fail(e, "p_attn launch");
     }
     return MHA_OK;

@@ -73,6 +73,7 @@ constexpr int kAttnStages = 4;     // K/V ring depth
 constexpr int kAttnThreads = 384;  // 2 softmax warpgroups (one per Q tile) + 1 warpgroup: TMA warp, 3 MMA warps
 
 struct AttnParams {
+    CUtensorMap p_map;     // p_attn kernel only: fp32 {L_k, L_q, B*h}, box {32, 128, 1} (when L_k % 4 == 0)
     CUtensorMap q_map;     // Qh as {64, L_q, B*h}
     CUtensorMap kv_map;    // KVh as {64, L_k, B*2h}
     CUtensorMap ctx_map;   // ctx as {d_model, L_q, B} (store)
@@ -86,6 +87,7 @@ struct AttnParams {
     int q_pairs;           // ceil(L_q / 256)
     int narrow_dk;         // d_k of heads narrower than 64 (8, 16, 32: q_map / kv_map zero-pad
                            // them to 64 columns, ctx_map stores d_k columns unswizzled); 0 otherwise
+    float* p_attn;         // p_attn kernel only: fp32 [B, h, L_q, L_k]
     int* status;
 };
 
@@ -94,21 +96,10 @@ cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t s);
 // d_k = 128: same parameters with q_map / kv_map as {64, 2, L, planes} and q_pairs = ceil(L_q / 128)
 cudaError_t launch_attn_tc_d128(const AttnParams& p, cudaStream_t s);
 
-// p_attn for the bf16 path from Qh, KVh and the row statistics.
-struct PattnParams {
-    const __nv_bfloat16* q;     // Qh [B, h, Lq, dk]
-    const __nv_bfloat16* kv;    // KVh [B, 2, h, Lk, dk]
-    int dk;                     // 64 or 128
-    const float* stats;         // [B, h, Lq, 2]
-    float* p_attn;              // [B, h, Lq, Lk]
-    int B, h, Lq, Lk;
-    int causal;
-    const int32_t* valid_lens;
-    const uint8_t* dense;
-    int dense_mq;
-    float scale_log2;
-};
-cudaError_t launch_pattn_bf16(const PattnParams& p, cudaStream_t s);
+// p_attn for the bf16 path (pattn_tc.cu): the scores recomputed on the tensor cores from
+// Qh and KVh (q_map, kv_map as for the attention), normalised with the row statistics
+// the attention kernel wrote (stats), written to p_attn. halves: 1 (d_k <= 64), 2 (d_k = 128).
+cudaError_t launch_pattn_tc(const AttnParams& p, int halves, cudaStream_t s);
 
 // ------------------------------------------------------------ diagnostics
 // One warp waits on an mbarrier nothing arrives on, through the bounded pipeline wait

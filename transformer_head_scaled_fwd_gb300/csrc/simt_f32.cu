@@ -80,6 +80,64 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(const F32GemmParams p) {
     }
 }
 
+// Few rows (M = B * L <= kSmallM, e.g. the tiny workload's 20 tokens): the tiled kernel
+// above would run a handful of CTAs through a long chain of dependent k-steps. Here one
+// warp owns one output feature n of one group and all rows: its lanes stream the weight
+// row and the input rows (consecutive k per lane, so every load is coalesced) four rows
+// at a time, and a butterfly reduction finishes each dot product.
+constexpr int kSmallM = 64;
+constexpr int kSmallWarps = 8;
+
+__device__ __forceinline__ float warp_sum_f32(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+constexpr int kSmallRows = 16;   // rows accumulated per pass
+
+__global__ void __launch_bounds__(32 * kSmallWarps) gemm_f32_small_m_kernel(const F32GemmParams p) {
+    const F32GemmGroup& G = p.g[blockIdx.y];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n = blockIdx.x * kSmallWarps + warp;
+    if (n >= p.N) return;   // whole warp
+    const long M = static_cast<long>(p.B) * G.L;
+    const float* w = G.W + static_cast<long>(n) * p.K;
+    const float bias = G.bias ? G.bias[n] : 0.0f;
+    for (long m0 = 0; m0 < M; m0 += kSmallRows) {
+        float acc[kSmallRows];
+#pragma unroll
+        for (int r = 0; r < kSmallRows; ++r) acc[r] = 0.f;
+        // unrolled so that the loads of several k-steps are in flight together
+#pragma unroll 4
+        for (int k = lane; k < p.K; k += 32) {
+            const float wk = w[k];
+#pragma unroll
+            for (int r = 0; r < kSmallRows; ++r)
+                if (m0 + r < M) acc[r] = fmaf(G.A[(m0 + r) * p.K + k], wk, acc[r]);
+        }
+#pragma unroll
+        for (int r = 0; r < kSmallRows; ++r) acc[r] = warp_sum_f32(acc[r]);
+        float mine = 0.f;   // lane r keeps row m0 + r's sum
+#pragma unroll
+        for (int r = 0; r < kSmallRows; ++r)
+            if (lane == r) mine = acc[r];
+        if (lane < kSmallRows && m0 + lane < M) {
+            const long m = m0 + lane;
+            float y = mine + bias;
+            if (p.relu) y = fmaxf(y, 0.0f);
+            if (G.residual) y += G.residual[m * p.N + n];
+            if (p.out_plain) {
+                G.out[m * p.N + n] = y;
+            } else {
+                const long b = m / G.L, l = m - b * G.L;
+                const int slab = G.out_j0 + n / p.dk;
+                G.out[((b * p.slabs + slab) * G.L + l) * p.dk + n % p.dk] = y;
+            }
+        }
+    }
+}
+
 constexpr int kMaxDk = 256;
 constexpr int kRowsPerBlock = 8;   // one warp per query row
 
@@ -173,6 +231,11 @@ cudaError_t launch_gemm_f32(const F32GemmParams& p, cudaStream_t s) {
     int maxL = 0;
     for (int g = 0; g < p.ngroups; ++g) maxL = max(maxL, p.g[g].L);
     const long M = static_cast<long>(p.B) * maxL;
+    if (M <= kSmallM) {
+        dim3 grid((p.N + kSmallWarps - 1) / kSmallWarps, p.ngroups);
+        gemm_f32_small_m_kernel<<<grid, 32 * kSmallWarps, 0, s>>>(p);
+        return cudaGetLastError();
+    }
     dim3 grid((p.N + kTN - 1) / kTN, static_cast<unsigned>((M + kTM - 1) / kTM), p.ngroups);
     gemm_f32_kernel<<<grid, 256, 0, s>>>(p);
     return cudaGetLastError();
