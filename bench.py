@@ -758,13 +758,14 @@ def run_gpu_decode(args):
     B.build()
     binding.load()
     peaks, peak_src = load_peaks()
-    Bn, d, h, P = args.decode_batch, 1024, 16, args.decode_context
+    Bn, d, h, P = args.decode_batch, 1024, args.decode_heads, args.decode_context
+    dk = d // h
     K, Wm = args.steps, args.warmup
     L_max = P + 2 * (K + Wm) + 8   # room for the direct loop and the graph replays
     inp = W.random_case(500 + rank, Bn, P + 1, P + 1, d, h, self_attn=True, bias_scale=0.0)
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda().to(torch.bfloat16)
     w = [dev(inp.weights[n]) for n in ("w_q", "b_q", "w_k", "b_k", "w_v", "b_v", "w_o", "b_o")]
-    kc = torch.zeros(Bn, h, L_max, 64, dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros(Bn, h, L_max, dk, dtype=torch.bfloat16, device="cuda")
     vc = torch.zeros_like(kc)
     binding.mha_kv_cache_prefill(dev(inp.query[:, :P]), w[2], w[3], w[4], w[5], h, k_cache=kc, v_cache=vc)
     clen = torch.full((Bn,), P, dtype=torch.int32, device="cuda")
@@ -801,15 +802,15 @@ def run_gpu_decode(args):
     ms = sum(a.elapsed_time(b) for a, b in evs[Wm:]) / K
     g_ms = sum(a.elapsed_time(b) for a, b in g_evs[Wm:]) / K
     mean_ctx = P + Wm + (K + 1) / 2.0          # cached tokens attended per step, on average
-    cache_bytes = Bn * h * mean_ctx * 64 * 2 * 2
-    bytes_step = cache_bytes + 4 * d * d * 2 + 4 * Bn * d * 2 + Bn * h * 64 * 2 * 2
+    cache_bytes = Bn * h * mean_ctx * dk * 2 * 2
+    bytes_step = cache_bytes + 4 * d * d * 2 + 4 * Bn * d * 2 + Bn * h * dk * 2 * 2
     gbs = bytes_step / (ms * 1e-3) / 1e9
     peak = float(peaks["hbm_gbs"])
     line = {
         "metric": "MHA incremental decode tokens/s (bf16, KV cache)", "value": Bn / (ms * 1e-3),
         "unit": "tokens/s", "n_gpus": 1, "steps": K, "warmup": Wm, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded)",
-        "config": {"workload": f"decode step B{Bn} d_model{d} h{h} d_k64, cache ~{P} tokens",
+        "config": {"workload": f"decode step B{Bn} d_model{d} h{h} d_k{dk}, cache ~{P} tokens",
                    "l2": "flushed before every step"},
         "roofline": {"kernel": "decode step (projection GEMMs + split-K cache attention)", "bound": "hbm",
                      "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak, "traffic": None,
@@ -835,6 +836,7 @@ def main():
                     help="skip the short records of the other workloads in the JSON line")
     ap.add_argument("--decode-batch", type=int, default=16)
     ap.add_argument("--decode-context", type=int, default=8192)
+    ap.add_argument("--decode-heads", type=int, default=16, help="heads at d_model 1024 (16: d_k 64, 8: d_k 128)")
     ap.add_argument("--path", choices=["mha", "ffn", "sublayer", "decode", "pattn"], default="mha",
                     help="mha: the attention sublayer (default); ffn: the position-wise FFN; "
                          "sublayer: x + MHA(LayerNorm(x)); decode: one token per sequence vs a KV cache; "

@@ -253,12 +253,12 @@ mha_status_t mha_sublayer_forward(mha_dtype_t dt, const void* x, const void* mem
                                   void* stream);
 
 /*
- * Incremental decoding with a key/value cache (bf16, d_k = 64 only).
+ * Incremental decoding with a key/value cache (bf16, d_k = 64 or 128).
  * At prediction time the d2l Transformer decoder (d2l Transformer chapter, DecoderBlock:
  * state[2] keeps the representations decoded so far and torch.cat appends the new one as
  * keys and values) attends from the newest token to every token so far, itself included.
  * This library caches the PROJECTED keys and values, which gives the same result.
- *   k_cache, v_cache  device [B, h, L_max, 64] bf16: position t of sequence b, head i.
+ *   k_cache, v_cache  device [B, h, L_max, d_k] bf16: position t of sequence b, head i.
  *   mha_kv_cache_prefill: projects x [B, T, d_model] into positions 0..T-1 of both caches
  *     (K = x W_k^T + b_k, V = x W_v^T + b_v); T <= L_max.
  *   mha_decode_step: one new token per sequence, x_new [B, d_model]:

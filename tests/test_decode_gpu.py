@@ -2,7 +2,7 @@
 
 Decoding a sequence one token at a time (each new token attends to every token
 so far, itself included: the d2l decoder at prediction time) must reproduce
-causal self-attention over the whole sequence, row by row."""
+causal self-attention over the whole sequence, row by row. Head widths 64 and 128."""
 import numpy as np
 import pytest
 
@@ -38,7 +38,7 @@ class Cache:
         h = inp.wl.h
         self.h = h
         self.w = [_dev(inp.weights[n]) for n in WN]
-        self.k = torch.zeros(B, h, L_max, 64, dtype=torch.bfloat16, device="cuda")
+        self.k = torch.zeros(B, h, L_max, d // h, dtype=torch.bfloat16, device="cuda")
         self.v = torch.zeros_like(self.k)
         self.len = torch.zeros(B, dtype=torch.int32, device="cuda")
         self.ws = torch.empty(bnd.decode_workspace_size(B, d, h, L_max), dtype=torch.uint8, device="cuda")
@@ -60,8 +60,9 @@ def _check(got, ref):
     assert np.all(err <= 1.5e-2 + 2e-2 * np.abs(ref)), f"max abs err {err.max():.3e}"
 
 
-def test_decode_from_empty_cache_equals_causal_attention(bnd):
-    B, T, d, h = 3, 40, 256, 4
+@pytest.mark.parametrize("h", [4, 2])   # d_k 64, 128
+def test_decode_from_empty_cache_equals_causal_attention(bnd, h):
+    B, T, d = 3, 40, 256
     inp = W.random_case(400, B, T, T, d, h, self_attn=True)
     c = Cache(bnd, inp, L_max=64)
     outs = [c.step(inp.query[:, t]) for t in range(T)]
@@ -74,8 +75,9 @@ def test_decode_from_empty_cache_equals_causal_attention(bnd):
     assert bnd.mha_check_device_status(reset=True) == 0
 
 
-def test_decode_after_prefill_with_ragged_histories(bnd):
-    B, T0, d, h = 3, 300, 512, 8
+@pytest.mark.parametrize("h", [8, 4])   # d_k 64, 128
+def test_decode_after_prefill_with_ragged_histories(bnd, h):
+    B, T0, d = 3, 300, 512
     inp = W.random_case(401, B, T0 + 1, T0 + 1, d, h, self_attn=True)
     c = Cache(bnd, inp, L_max=512)
     c.prefill(inp.query[:, :T0])
@@ -94,9 +96,10 @@ def test_decode_after_prefill_with_ragged_histories(bnd):
     assert bnd.mha_check_device_status(reset=True) == 0
 
 
-def test_decode_long_cache(bnd):
-    """The bench's cache length (8192) with d_model 1024, h 16, on two sequences."""
-    B, T0, d, h = 2, 8192, 1024, 16
+@pytest.mark.parametrize("h", [16, 8])   # d_k 64, 128
+def test_decode_long_cache(bnd, h):
+    """The bench's cache length (8192) with d_model 1024, on two sequences."""
+    B, T0, d = 2, 8192, 1024
     inp = W.random_case(402, B, T0 + 1, T0 + 1, d, h, self_attn=True, bias_scale=0.0)
     c = Cache(bnd, inp, L_max=T0 + 64)
     c.prefill(inp.query[:, :T0])
@@ -108,8 +111,9 @@ def test_decode_long_cache(bnd):
     assert bnd.mha_check_device_status(reset=True) == 0
 
 
-def test_full_cache_is_reported_not_written(bnd):
-    B, d, h = 2, 128, 2
+@pytest.mark.parametrize("d", [128, 256])   # d_k 64, 128
+def test_full_cache_is_reported_not_written(bnd, d):
+    B, h = 2, 2
     inp = W.random_case(403, B, 8, 8, d, h, self_attn=True)
     c = Cache(bnd, inp, L_max=8)
     c.prefill(inp.query)
@@ -121,12 +125,13 @@ def test_full_cache_is_reported_not_written(bnd):
     assert bnd.mha_check_device_status(reset=True) == 0x301
 
 
-@pytest.mark.parametrize("B", [17, 40, 64, 70])
-def test_decode_batch_sizes(bnd, B):
+@pytest.mark.parametrize("B,h", [(17, 8), (40, 8), (64, 8), (70, 8), (40, 4), (70, 4)])
+def test_decode_batch_sizes(bnd, B, h):
     """Projections of the step: up to 64 new tokens stream W over many CTAs in passes of
-    16 rows (17, 40: a partial last pass); 70 tokens use the tiled projection GEMM."""
-    T0, d, h = 100, 512, 8
-    inp = W.random_case(410 + B, B, T0 + 1, T0 + 1, d, h, self_attn=True, bias_scale=0.1)
+    16 rows (17, 40: a partial last pass); 70 tokens use the tiled projection GEMM.
+    h 8 / 4 at d_model 512: d_k 64 / 128."""
+    T0, d = 100, 512
+    inp = W.random_case(410 + B + h, B, T0 + 1, T0 + 1, d, h, self_attn=True, bias_scale=0.1)
     c = Cache(bnd, inp, L_max=128)
     c.prefill(inp.query[:, :T0])
     got = c.step(inp.query[:, T0])

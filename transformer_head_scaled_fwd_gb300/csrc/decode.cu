@@ -37,16 +37,16 @@
 namespace mha {
 namespace {
 
-constexpr int kD = 64;
 constexpr int kWarps = 4;
 
+template <int kD>
 __global__ void __launch_bounds__(256) kv_append_kernel(const DecodeParams p) {
     pdl_trigger();
     pdl_wait();
     const int b = blockIdx.x;
     const int pos = p.cache_len[b];
     if (pos < 0 || pos >= p.L_max) return;   // full cache: nothing appended (reported by the combine)
-    // KVh of the step is [1, 2, h, B, 64]: k of (b, head) at ((head) * B + b) * 64, v after h planes
+    // KVh of the step is [1, 2, h, B, D]: k of (b, head) at ((head) * B + b) * D, v after h planes
     for (int e = threadIdx.x; e < p.h * kD / 8; e += blockDim.x) {
         const int head = e / (kD / 8);
         const int c8 = e % (kD / 8);
@@ -69,7 +69,15 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Head width kD = 64 or 128. A key (value) row is kD * 2 bytes: kLanesRow = kD / 8 lanes
+// read it with one 16-byte load each, so one load instruction of a warp reads kRowsLoad
+// whole consecutive rows (512 contiguous bytes); each lane loads 8 rows per group, so a
+// group is kGroup = 8 * kRowsLoad keys.
+template <int kD>
 __global__ void __launch_bounds__(32 * kWarps) decode_attn_kernel(const DecodeParams p) {
+    constexpr int kLanesRow = kD / 8;
+    constexpr int kRowsLoad = 32 / kLanesRow;
+    constexpr int kGroup = 8 * kRowsLoad;
     __shared__ float sm_m[kWarps], sm_l[kWarps];
     __shared__ float sm_o[kWarps][kD];
     pdl_trigger();
@@ -100,11 +108,10 @@ __global__ void __launch_bounds__(32 * kWarps) decode_attn_kernel(const DecodePa
     const int chunk = ((n + p.n_split - 1) / p.n_split + 31) & ~31;
     const int c0 = blockIdx.x * chunk;
     const int c1 = min(n, c0 + chunk);
-    // Lane (grp, sl) = (lane / 8, lane % 8) holds dims 8 sl .. 8 sl + 7 of the keys
-    // 4 i + grp (i = 0..7) of each group of 32: every load instruction of the warp
-    // reads 4 whole consecutive key (or value) rows, 512 contiguous bytes.
-    const int grp = lane >> 3;
-    const int sl = lane & 7;
+    // Lane (grp, sl) = (lane / kLanesRow, lane % kLanesRow) holds dims 8 sl .. 8 sl + 7 of
+    // the keys kRowsLoad i + grp (i = 0..7) of each group.
+    const int grp = lane / kLanesRow;
+    const int sl = lane % kLanesRow;
 
     // this lane's slice of the query row, pre-scaled so that scores are in log2 units
     float q[8];
@@ -124,17 +131,17 @@ __global__ void __launch_bounds__(32 * kWarps) decode_attn_kernel(const DecodePa
     float o[8];   // partial p.V over this lane's keys, dims 8 sl ..
 #pragma unroll
     for (int f = 0; f < 8; ++f) o[f] = 0.0f;
-    for (int g0 = c0 + 32 * warp; g0 < c1; g0 += 32 * kWarps) {
+    for (int g0 = c0 + kGroup * warp; g0 < c1; g0 += kGroup * kWarps) {
         // keys and values of the group, all 16 loads in flight together
         uint4 kr[8], vr[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const int key = g0 + 4 * i + grp;
+            const int key = g0 + kRowsLoad * i + grp;
             kr[i] = (key < c1) ? *reinterpret_cast<const uint4*>(K + static_cast<long>(key) * kD) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const int key = g0 + 4 * i + grp;
+            const int key = g0 + kRowsLoad * i + grp;
             vr[i] = (key < c1) ? *reinterpret_cast<const uint4*>(V + static_cast<long>(key) * kD) : make_uint4(0, 0, 0, 0);
         }
         // partial scores of the 8 keys over this lane's 8 dims
@@ -151,8 +158,8 @@ __global__ void __launch_bounds__(32 * kWarps) decode_attn_kernel(const DecodePa
             }
             part[i] = a;
         }
-        // reduce-scatter over the 8 lanes of the group: lane sl ends with the whole score
-        // of its key i = sl, i.e. key g0 + 4 sl + grp
+        // reduce-scatter over 8 lanes of the row: lane sl ends with key i = sl % 8's score
+        // summed over those lanes (for kD = 128 the two halves of the row are then added)
 #pragma unroll
         for (int s = 4; s >= 1; s >>= 1) {
             const bool upper = (sl & s) != 0;
@@ -163,17 +170,22 @@ __global__ void __launch_bounds__(32 * kWarps) decode_attn_kernel(const DecodePa
                 part[t] = keep + __shfl_xor_sync(0xffffffffu, send, s);
             }
         }
-        const float sc = (g0 + 4 * sl + grp < c1) ? part[0] : -CUDART_INF_F;
+        if constexpr (kLanesRow == 16) part[0] += __shfl_xor_sync(0xffffffffu, part[0], 8);
+        // the lane holds key g0 + kRowsLoad (sl % 8) + grp; with kD = 128 lanes sl and sl + 8
+        // hold the same key, and only the first counts in the sums
+        const bool owner = sl < 8;
+        const float sc = (g0 + kRowsLoad * (sl & 7) + grp < c1) ? part[0] : -CUDART_INF_F;
         const float m_new = fmaxf(m, warp_max(sc));   // finite: key g0 < c1 always exists
         const float alpha = ex2_approx(m - m_new);
         const float pj = ex2_approx(sc - m_new);      // 0 for keys past the chunk
-        l = l * alpha + warp_sum(pj);
+        l = l * alpha + warp_sum(owner ? pj : 0.0f);
 #pragma unroll
         for (int f = 0; f < 8; ++f) o[f] *= alpha;
-        // this lane's value rows are keys 4 i + grp, whose weights sit in lanes 8 grp + i
+        // this lane's value rows are keys kRowsLoad i + grp, whose weights sit in lanes
+        // kLanesRow grp + i
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const float w = __shfl_sync(0xffffffffu, pj, 8 * grp + i);
+            const float w = __shfl_sync(0xffffffffu, pj, kLanesRow * grp + i);
             const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&vr[i]);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -184,43 +196,47 @@ __global__ void __launch_bounds__(32 * kWarps) decode_attn_kernel(const DecodePa
         }
         m = m_new;
     }
-    // lanes with the same dims (sl) hold partials over disjoint keys: sum the 4 groups
+    // lanes with the same dims (sl) hold partials over disjoint keys: sum the groups
 #pragma unroll
     for (int f = 0; f < 8; ++f) {
-        o[f] += __shfl_xor_sync(0xffffffffu, o[f], 8);
-        o[f] += __shfl_xor_sync(0xffffffffu, o[f], 16);
+#pragma unroll
+        for (int x = kLanesRow; x < 32; x <<= 1) o[f] += __shfl_xor_sync(0xffffffffu, o[f], x);
     }
     if (lane == 0) {
         sm_m[warp] = m;
         sm_l[warp] = l;
     }
-    if (lane < 8) {
+    if (lane < kLanesRow) {
 #pragma unroll
         for (int f = 0; f < 8; ++f) sm_o[warp][8 * lane + f] = o[f];
     }
     __syncthreads();
     if (warp == 0) {
+        constexpr int kPer = kD / 32;   // output dims per lane
         float M = -CUDART_INF_F;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w]);
-        float L = 0.0f, a0 = 0.0f, a1 = 0.0f;
+        float L = 0.0f, a[kPer];
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) a[e] = 0.0f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
             const float f = (sm_m[w] == -CUDART_INF_F) ? 0.0f : ex2_approx(sm_m[w] - M);
             L += sm_l[w] * f;
-            a0 += sm_o[w][2 * lane] * f;
-            a1 += sm_o[w][2 * lane + 1] * f;
+#pragma unroll
+            for (int e = 0; e < kPer; ++e) a[e] += sm_o[w][kPer * lane + e] * f;
         }
         float* part = p.partial + (static_cast<long>(bh) * p.n_split + blockIdx.x) * (kD + 2);
         if (lane == 0) {
             part[0] = M;
             part[1] = L;
         }
-        part[2 + 2 * lane] = a0;
-        part[3 + 2 * lane] = a1;
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) part[2 + kPer * lane + e] = a[e];
     }
 }
 
+template <int kD>
 __global__ void __launch_bounds__(kD) decode_combine_kernel(const DecodeParams p) {
     pdl_trigger();
     pdl_wait();
@@ -264,13 +280,19 @@ __global__ void __launch_bounds__(kD) decode_combine_kernel(const DecodeParams p
 }  // namespace
 
 cudaError_t launch_kv_append(const DecodeParams& p, cudaStream_t s) {
-    return launch_pdl(kv_append_kernel, dim3(p.B), dim3(256), 0, s, p);
+    if (p.dk == 128) return launch_pdl(kv_append_kernel<128>, dim3(p.B), dim3(256), 0, s, p);
+    return launch_pdl(kv_append_kernel<64>, dim3(p.B), dim3(256), 0, s, p);
+}
+
+template <int kD>
+cudaError_t launch_decode_attention_d(const DecodeParams& p, cudaStream_t s) {
+    cudaError_t e = launch_pdl(decode_attn_kernel<kD>, dim3(p.n_split, p.B * p.h), dim3(32 * kWarps), 0, s, p);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(decode_combine_kernel<kD>, dim3(p.B * p.h), dim3(kD), 0, s, p);
 }
 
 cudaError_t launch_decode_attention(const DecodeParams& p, cudaStream_t s) {
-    cudaError_t e = launch_pdl(decode_attn_kernel, dim3(p.n_split, p.B * p.h), dim3(32 * kWarps), 0, s, p);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(decode_combine_kernel, dim3(p.B * p.h), dim3(kD), 0, s, p);
+    return p.dk == 128 ? launch_decode_attention_d<128>(p, s) : launch_decode_attention_d<64>(p, s);
 }
 
 }  // namespace mha

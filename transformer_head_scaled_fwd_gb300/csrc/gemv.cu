@@ -136,12 +136,12 @@ __global__ void __launch_bounds__(32 * kGemvWarps) gemv_bf16_kernel(const __grid
             if (g > 0 && p.k_cache != nullptr) {   // the step's key / value: straight into the cache
                 const int pos = pos_out;
                 if (pos >= 0 && pos < p.L_max)
-                    (g == 1 ? p.k_cache : p.v_cache)[((static_cast<long>(m) * (p.N / 64) + n / 64) * p.L_max + pos) *
-                                                          64 + (n & 63)] = __float2bfloat16_rn(y);
+                    (g == 1 ? p.k_cache : p.v_cache)[((static_cast<long>(m) * (p.N / p.dk) + n / p.dk) * p.L_max + pos) *
+                                                          p.dk + n % p.dk] = __float2bfloat16_rn(y);
             } else {
                 long off;
-                if (p.head_split)   // plane j0 + n / 64, row m, column n % 64 of [planes, M, 64]
-                    off = (static_cast<long>(p.j0[g] + n / 64) * p.M + m) * 64 + (n & 63);
+                if (p.head_split)   // plane j0 + n / dk, row m, column n % dk of [planes, M, dk]
+                    off = (static_cast<long>(p.j0[g] + n / p.dk) * p.M + m) * p.dk + n % p.dk;
                 else
                     off = static_cast<long>(m) * p.N + n;
                 p.out[g][off] = __float2bfloat16_rn(y);

@@ -13,12 +13,13 @@ struct GemvParams {
     const __nv_bfloat16* x;          // [M, K]
     const __nv_bfloat16* w[3];       // [N, K] each
     const __nv_bfloat16* bias[3];    // [N] or nullptr
-    __nv_bfloat16* out[3];           // head-split [planes, M, 64] or plain [M, N]
+    __nv_bfloat16* out[3];           // head-split [planes, M, dk] or plain [M, N]
     int j0[3];                       // head-split: first plane of this matrix's output
     int M, N, K, ngroups;
     int head_split;
+    int dk;                          // head width (64 or 128) of the head-split and cache layouts
     // Key/value caches (decode): when k_cache != nullptr, matrices 1 and 2 write row m
-    // (sequence m) into k_cache / v_cache [M, N / 64, L_max, 64] at position
+    // (sequence m) into k_cache / v_cache [M, N / dk, L_max, dk] at position
     // cache_len[m] instead of out[1] / out[2]; nothing is written when that position
     // is not below L_max (full cache).
     __nv_bfloat16* k_cache;

@@ -732,7 +732,7 @@ static int decode_split(int B, int h, int L_max) {
 size_t mha_decode_workspace_size(int B, int d_model, int h, int L_max) {
     if (B <= 0 || d_model <= 0 || h <= 0 || L_max <= 0 || d_model % h != 0) return 0;
     const size_t ws = mha_workspace_size(MHA_BF16, 1, B, B, d_model, h);
-    return ws + align256(sizeof(float) * (mha::kAttnD + 2) * B * h * static_cast<size_t>(mha::kDecodeMaxSplit));
+    return ws + align256(sizeof(float) * (d_model / h + 2) * B * h * static_cast<size_t>(mha::kDecodeMaxSplit));
 }
 
 mha_status_t mha_kv_cache_prefill(mha_dtype_t dt, const void* x, const void* w_k, const void* b_k, const void* w_v,
@@ -741,7 +741,9 @@ mha_status_t mha_kv_cache_prefill(mha_dtype_t dt, const void* x, const void* w_k
     if (dt != MHA_BF16) return fail(MHA_ERR_UNSUPPORTED, "the key/value cache is implemented for bf16 only");
     mha_status_t st = check_sizes(dt, B, T, T, d_model, h);
     if (st != MHA_OK) return st;
-    if (d_model / h != 64) return fail(MHA_ERR_UNSUPPORTED, "the key/value cache is implemented for d_k = 64");
+    const int dk = d_model / h;
+    if (dk != 64 && dk != 128)
+        return fail(MHA_ERR_UNSUPPORTED, "the key/value cache is implemented for d_k = 64 and 128 (d_k = %d)", dk);
     if (T > L_max) return fail(MHA_ERR_INVALID_ARG, "T (%d) exceeds the cache length L_max (%d)", T, L_max);
     if (!x || !w_k || !w_v || !k_cache || !v_cache)
         return fail(MHA_ERR_INVALID_ARG, "x, W_k, W_v and the caches must not be NULL");
@@ -756,7 +758,7 @@ mha_status_t mha_kv_cache_prefill(mha_dtype_t dt, const void* x, const void* w_k
     void* cache[2] = {k_cache, v_cache};
     for (int g = 0; g < 2; ++g) {
         if ((st = map_rows(&p.a[g], x, B, T, d_model, "prefill input")) != MHA_OK) return st;
-        if ((st = map_heads5(&p.out[g], cache[g], B, h, T, 1, L_max)) != MHA_OK) return st;
+        if ((st = map_heads5(&p.out[g], cache[g], B, h, T, dk / 64, L_max)) != MHA_OK) return st;
         p.g[g].L = T;
         p.g[g].tiles_per_b = (T + mha::kGemmBM - 1) / mha::kGemmBM;
         p.g[g].m_tiles = B * p.g[g].tiles_per_b;
@@ -766,7 +768,7 @@ mha_status_t mha_kv_cache_prefill(mha_dtype_t dt, const void* x, const void* w_k
     p.ngroups = 2;
     p.K = d_model;
     p.N = d_model;
-    p.dk_slabs = 1;
+    p.dk_slabs = dk / 64;
     p.status = device_status_ptr();
     if (!p.status) return fail(MHA_ERR_CUDA, "device status word unavailable");
     return launch_projection(p, W, as_stream(stream), "cache prefill launch");
@@ -779,7 +781,9 @@ mha_status_t mha_decode_step(mha_dtype_t dt, const void* x_new, const void* w_q,
     if (dt != MHA_BF16) return fail(MHA_ERR_UNSUPPORTED, "incremental decoding is implemented for bf16 only");
     mha_status_t st = check_sizes(dt, 1, B, B, d_model, h);
     if (st != MHA_OK) return st;
-    if (d_model / h != 64) return fail(MHA_ERR_UNSUPPORTED, "incremental decoding is implemented for d_k = 64");
+    const int dk = d_model / h;
+    if (dk != 64 && dk != 128)
+        return fail(MHA_ERR_UNSUPPORTED, "incremental decoding is implemented for d_k = 64 and 128 (d_k = %d)", dk);
     if (L_max <= 0) return fail(MHA_ERR_INVALID_ARG, "L_max must be positive");
     if (!x_new || !w_q || !w_k || !w_v || !w_o || !k_cache || !v_cache || !cache_len || !out)
         return fail(MHA_ERR_INVALID_ARG, "x_new, weights, caches, cache_len and out must not be NULL");
@@ -809,7 +813,7 @@ mha_status_t mha_decode_step(mha_dtype_t dt, const void* x_new, const void* w_q,
         g.out[0] = reinterpret_cast<__nv_bfloat16*>(ws + L.q);
         g.out[1] = g.out[2] = reinterpret_cast<__nv_bfloat16*>(ws + L.kv);
         g.j0[0] = 0; g.j0[1] = 0; g.j0[2] = h;
-        g.M = B; g.N = d_model; g.K = d_model; g.ngroups = 3; g.head_split = 1;
+        g.M = B; g.N = d_model; g.K = d_model; g.ngroups = 3; g.head_split = 1; g.dk = dk;
         g.k_cache = static_cast<__nv_bfloat16*>(k_cache);   // k, v of the step go straight to the caches
         g.v_cache = static_cast<__nv_bfloat16*>(v_cache);
         g.cache_len = cache_len;
@@ -828,11 +832,12 @@ mha_status_t mha_decode_step(mha_dtype_t dt, const void* x_new, const void* w_q,
     p.cache_len = cache_len;
     p.ctx = reinterpret_cast<__nv_bfloat16*>(ws + L.ctx);
     p.partial = reinterpret_cast<float*>(ws + ws_mha);
+    p.dk = dk;
     p.B = B;
     p.h = h;
     p.L_max = L_max;
     p.n_split = decode_split(B, h, L_max);
-    p.scale_log2 = static_cast<float>(1.4426950408889634 / 8.0);
+    p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(dk)));
     p.status = device_status_ptr();
     if (!p.status) return fail(MHA_ERR_CUDA, "device status word unavailable");
     // keys each attention CTA prefetches into L2 while the small-M projections run: an eighth
@@ -840,7 +845,7 @@ mha_status_t mha_decode_step(mha_dtype_t dt, const void* x_new, const void* w_q,
     if (gemv) {
         const long ctas = static_cast<long>(p.n_split) * B * h;
         const long chunk = (L_max + p.n_split - 1) / p.n_split;
-        p.prefetch_keys = static_cast<int>(std::min<long>(chunk / 8, (64l << 20) / (ctas * 2 * 64 * 2)));
+        p.prefetch_keys = static_cast<int>(std::min<long>(chunk / 8, (64l << 20) / (ctas * 2 * dk * 2)));
     }
     const cudaStream_t s = as_stream(stream);
     // 2. (tiled projections only) append k, v at cache_len[b]; 3. attention over the cache,
@@ -856,7 +861,7 @@ mha_status_t mha_decode_step(mha_dtype_t dt, const void* x_new, const void* w_q,
         g.w[0] = static_cast<const __nv_bfloat16*>(w_o);
         g.bias[0] = static_cast<const __nv_bfloat16*>(b_o);
         g.out[0] = static_cast<__nv_bfloat16*>(out);
-        g.M = B; g.N = d_model; g.K = d_model; g.ngroups = 1; g.head_split = 0;
+        g.M = B; g.N = d_model; g.K = d_model; g.ngroups = 1; g.head_split = 0; g.dk = dk;
         e = mha::launch_gemv_bf16(g, s);
         if (e != cudaSuccess) return cuda_fail(e, "decode output projection launch");
         return MHA_OK;

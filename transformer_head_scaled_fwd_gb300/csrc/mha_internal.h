@@ -140,15 +140,16 @@ struct F32AttnParams {
 };
 cudaError_t launch_attn_f32(const F32AttnParams& p, cudaStream_t s);
 
-// ------------------------------------------------------------ incremental decoding (d_k = 64, bf16)
+// ------------------------------------------------------------ incremental decoding (d_k = 64 or 128, bf16)
 struct DecodeParams {
-    const __nv_bfloat16* q_new;    // Qh of the step [1, h, B, 64]
-    const __nv_bfloat16* kv_new;   // KVh of the step [1, 2, h, B, 64] (tiled projections only)
-    __nv_bfloat16* k_cache;        // [B, h, L_max, 64]
-    __nv_bfloat16* v_cache;        // [B, h, L_max, 64]
+    const __nv_bfloat16* q_new;    // Qh of the step [1, h, B, dk]
+    const __nv_bfloat16* kv_new;   // KVh of the step [1, 2, h, B, dk] (tiled projections only)
+    __nv_bfloat16* k_cache;        // [B, h, L_max, dk]
+    __nv_bfloat16* v_cache;        // [B, h, L_max, dk]
     int32_t* cache_len;            // [B]; the step's token sits at cache_len[b], counted by the combine kernel
-    __nv_bfloat16* ctx;            // [1, B, h * 64]
-    float* partial;                // [B * h, n_split, 66]: max (log2 units), sum, o[64]
+    __nv_bfloat16* ctx;            // [1, B, h * dk]
+    float* partial;                // [B * h, n_split, dk + 2]: max (log2 units), sum, o[dk]
+    int dk;                        // 64 or 128
     int B, h, L_max, n_split;
     float scale_log2;
     int* status;
