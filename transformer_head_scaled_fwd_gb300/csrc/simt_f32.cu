@@ -22,7 +22,7 @@ namespace {
 
 constexpr int kTM = 64, kTN = 64, kTK = 16;   // block tile; 256 threads x (4 x 4) outputs
 
-__global__ void __launch_bounds__(256) gemm_f32_kernel(const F32GemmParams p) {
+__global__ void __launch_bounds__(256) gemm_f32_kernel(const __grid_constant__ F32GemmParams p) {
     const F32GemmGroup& G = p.g[blockIdx.z];
     const long M = static_cast<long>(p.B) * G.L;
     const long m0 = static_cast<long>(blockIdx.y) * kTM;
@@ -96,25 +96,29 @@ __device__ __forceinline__ float warp_sum_f32(float v) {
 
 constexpr int kSmallRows = 16;   // rows accumulated per pass
 
-__global__ void __launch_bounds__(32 * kSmallWarps) gemm_f32_small_m_kernel(const F32GemmParams p) {
+__global__ void __launch_bounds__(32 * kSmallWarps) gemm_f32_small_m_kernel(const __grid_constant__ F32GemmParams p) {
     const F32GemmGroup& G = p.g[blockIdx.y];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n = blockIdx.x * kSmallWarps + warp;
     if (n >= p.N) return;   // whole warp
+    const int K = p.K;
     const long M = static_cast<long>(p.B) * G.L;
-    const float* w = G.W + static_cast<long>(n) * p.K;
+    const float* __restrict__ A = G.A;
+    const float* __restrict__ w = G.W + static_cast<long>(n) * K;
     const float bias = G.bias ? G.bias[n] : 0.0f;
     for (long m0 = 0; m0 < M; m0 += kSmallRows) {
         float acc[kSmallRows];
 #pragma unroll
         for (int r = 0; r < kSmallRows; ++r) acc[r] = 0.f;
         // unrolled so that the loads of several k-steps are in flight together
+        const int rows = static_cast<int>(min(static_cast<long>(kSmallRows), M - m0));
+        const float* __restrict__ a0 = A + m0 * K;
 #pragma unroll 4
-        for (int k = lane; k < p.K; k += 32) {
-            const float wk = w[k];
+        for (int k = lane; k < K; k += 32) {
+            const float wk = __ldg(w + k);
 #pragma unroll
             for (int r = 0; r < kSmallRows; ++r)
-                if (m0 + r < M) acc[r] = fmaf(G.A[(m0 + r) * p.K + k], wk, acc[r]);
+                if (r < rows) acc[r] = fmaf(__ldg(a0 + static_cast<long>(r) * K + k), wk, acc[r]);
         }
 #pragma unroll
         for (int r = 0; r < kSmallRows; ++r) acc[r] = warp_sum_f32(acc[r]);
@@ -152,7 +156,7 @@ __device__ __forceinline__ bool allowed_f32(const F32AttnParams& p, int b, int q
     return true;
 }
 
-__global__ void __launch_bounds__(32 * kRowsPerBlock) attn_f32_kernel(const F32AttnParams p) {
+__global__ void __launch_bounds__(32 * kRowsPerBlock) attn_f32_kernel(const __grid_constant__ F32AttnParams p) {
     __shared__ float qs[kRowsPerBlock][kMaxDk];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bh = blockIdx.y;
