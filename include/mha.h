@@ -85,6 +85,8 @@ typedef struct {
  *   KVh  [B, 2, h, L_k, d_k]   head-split projected keys (slot 0) and values (slot 1)
  *   ctx  [B, L_q, d_model]     concatenated head outputs (input of W_o)
  *   stat [B, h, L_q, 2] fp32   per-row softmax statistics (max, sum) used for p_attn
+ *   sched 256 bytes            2 ints: the d_k = 128 attention's work counter (zeroed by the
+ *                              Q/K/V projection stage, left at zero by the attention stage)
  * For MHA_BF16 with a d_k the tensor-core kernels do not take (d_k <= 256): the MHA_F32
  * workspace of the same sizes, then fp32 copies of query, key, value [B, L, d_model], of
  * the four weights and biases and of out, each 256-byte aligned.

@@ -37,7 +37,7 @@ def test_version(lib):
 
 
 def test_workspace_size_layout(lib):
-    # bf16: Qh + KVh + ctx + stats, each 256-aligned
+    # bf16: Qh + KVh + ctx + stats, each 256-aligned, then 256 bytes of schedule counter
     B_, Lq, Lk, d, h = 2, 10, 7, 512, 8
     es = 2
     a = lambda x: (x + 255) // 256 * 256
@@ -45,7 +45,7 @@ def test_workspace_size_layout(lib):
     kv = a(es * B_ * 2 * Lk * d)
     ctx = a(es * B_ * Lq * d)
     st = a(4 * 2 * B_ * h * Lq)
-    assert binding.workspace_size(binding.MHA_BF16, B_, Lq, Lk, d, h) == q + kv + ctx + st
+    assert binding.workspace_size(binding.MHA_BF16, B_, Lq, Lk, d, h) == q + kv + ctx + st + 256
     assert binding.workspace_size(binding.MHA_BF16, B_, Lq, Lk, 510, 8) == 0
     assert binding.workspace_size(binding.MHA_F32, 0, Lq, Lk, d, h) == 0
 

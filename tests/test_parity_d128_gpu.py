@@ -65,3 +65,37 @@ def test_d128_full_size_causal_sampled_rows():
     got, _ = run_gpu(inp, causal=True)
     ref = run_oracle(inp, causal=True, rows=rows)
     assert_close(got[:, rows], ref, "bf16")
+
+
+def test_d128_work_counter_reset_and_reuse():
+    """The d_k = 128 attention is persistent: its CTAs draw query tiles from a counter in
+    the workspace. With the workspace filled with 0xFF first (the projection stage zeroes
+    the counter) and the attention stage run three times after one projection (each
+    launch leaves the counter at zero), every run gives the same context bit for bit,
+    close to the oracle, and the counter words end at zero. 256 query tiles: more than one
+    per SM."""
+    from gpu_helpers import to_dev
+    from transformer_head_scaled_fwd_gb300 import binding
+    inp = W.random_case(630, 8, 1000, 1000, 512, 4, self_attn=True)
+    B, L, d, h = 8, 1000, 512, 4
+    dt = torch.bfloat16
+    x = to_dev(inp.query, dt)
+    Wt = {n: to_dev(a, dt) for n, a in inp.weights.items()}
+    size = binding.workspace_size(binding.MHA_BF16, B, L, L, d, h)
+    ws = torch.full((size,), 255, dtype=torch.uint8, device="cuda")
+    mask = binding.make_mask(True, None, None)
+    binding.mha_qkv_projection(x, x, x, Wt["w_q"], Wt["b_q"], Wt["w_k"], Wt["b_k"], Wt["w_v"], Wt["b_v"], h,
+                               workspace=ws)
+    outs = []
+    for _ in range(3):
+        out = torch.empty(B, L, d, dtype=dt, device="cuda")
+        binding.mha_attention_core(binding.MHA_BF16, B, L, L, d, h, workspace=ws, mask=mask)
+        binding.mha_output_projection(Wt["w_o"], Wt["b_o"], B, L, L, h, out=out, workspace=ws)
+        outs.append(out)
+    torch.cuda.synchronize()
+    assert binding.mha_check_device_status(reset=True) == 0
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    assert ws[size - 256:size - 248].view(torch.int32).tolist() == [0, 0]
+    rows = W.sample_rows(L, 48, seed=631)
+    ref = run_oracle(inp, causal=True, rows=rows)
+    assert_close(outs[0].double().cpu().numpy()[:, rows], ref, "bf16")

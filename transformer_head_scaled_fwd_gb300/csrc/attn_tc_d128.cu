@@ -4,7 +4,7 @@
 // "Attention", attention(): scores / sqrt(d_k), masked_fill(mask == 0, -1e9),
 // softmax over keys, P.V; the head's output written into its slab of the
 // concatenated context), for heads of width 128 (e.g. d_model 1024 with h = 8).
-// CTA = one 128-row query tile of one (batch, head); key tiles of 128.
+// Unit of work = one 128-row query tile of one (batch, head); key tiles of 128.
 //
 // Each query row is shared by two softmax threads: thread (h, row) of warpgroup h
 // takes keys 64 h .. 64 h + 63 of every key tile and keeps its own running max m_h,
@@ -20,21 +20,32 @@
 // tensor pipe (S = Q K^T and P.V, 8 MMAs of N = 128 each per key tile) no longer
 // waits on a single warp's softmax.
 //
+// Persistent: one CTA per SM draws query tiles ("units": (batch, head, 128 query rows))
+// from a counter in the workspace, in the order (groups of kHeadGroup (batch, head)
+// pairs, longest query tiles first), so the K/V in flight fit L2 and the short tiles
+// fill the end. The next unit's Q, K and V tiles are loaded, and its first score tile
+// computed, while the current unit's softmax and output finish: a CTA's set-up is paid
+// once, not once per query tile. The last CTA to finish resets the counter; the Q/K/V
+// projection kernel also zeroes it before the first use of a workspace.
+//
 // Tensor memory (512 columns):
 //   S    [0,128)    fp32 scores of the current key tile (released as soon as both
 //                   halves have loaded them: S(j+1) is computed during softmax(j))
 //   P    [128,192)  bf16 weights, P_0 (keys 0..63) in [128,160), P_1 in [160,192)
 //   O_0  [256,384)  fp32 output accumulator of key half 0 (128 features)
 //   O_1  [384,512)  fp32 output accumulator of key half 1
-// Shared memory: Q (two 64-wide 128-byte-swizzled halves), K and V rings of 3
-// stages (each tile two halves). S = Q K^T is SS-MMA M=128 N=128 (8 k-steps);
-// O_h += P_h V_h takes P_h from tensor memory and the 64 value rows of half h
-// MN-major with N = 128 (the two 64-wide feature halves are the descriptor's two
-// MN blocks, LBO apart): 4 k-steps per half.
-// Warps: 0-3 / 4-7 softmax of key half 0 / 1 (one thread per query row), 8 TMA,
-// 9 score MMAs (and tensor-memory allocation), 10 P.V MMAs, 11 idle. Registers:
-// 168 per thread at launch; the third warpgroup drops to 64 and the softmax
+// Shared memory: two Q buffers (unit u uses buffer u mod 2; after its last score MMA
+// the buffer stages the unit's output for the TMA store), a K ring of 3 stages and a
+// V ring of 2 (every tile two 64-wide 128-byte-swizzled halves). S = Q K^T is SS-MMA
+// M=128 N=128 (8 k-steps); O_h += P_h V_h takes P_h from tensor memory and the 64 value
+// rows of half h MN-major with N = 128 (the two 64-wide feature halves are the
+// descriptor's two MN blocks, LBO apart): 4 k-steps per half.
+// Warps: 0-3 / 4-7 softmax of key half 0 / 1 (one thread per query row), 8 scheduler
+// and Q/K loads, 9 score MMAs (and tensor-memory allocation), 10 P.V MMAs, 11 V loads.
+// Registers: 168 per thread at launch; the third warpgroup drops to 64 and the softmax
 // warpgroups rise to 216 (128*64 + 256*216 = 63488 <= 384*168).
+#include <algorithm>
+
 #include <math_constants.h>
 
 #include "launch.h"
@@ -47,7 +58,8 @@ namespace {
 constexpr int D = 128;
 constexpr int BM = 128;
 constexpr int BN = 128;
-constexpr int kStages = 3;
+constexpr int kStagesK = 3;
+constexpr int kStagesV = 2;
 constexpr int kThreads = 384;
 constexpr uint32_t kHalf = 128 * 128;        // one 128-row x 64-column bf16 half tile = 16 KB
 constexpr uint32_t kTile = 2 * kHalf;        // 128 x 128 bf16
@@ -59,61 +71,77 @@ constexpr float kMaskedLog2 = -1.0e9f * 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;
 constexpr int kHeadGroup = 8;
 
+// One unit as the scheduler publishes it; n == 0 means no more work.
+struct UnitInfo {
+    int b, head, q0, n, vl;
+};
+
 struct Smem128 {
-    uint64_t q_full;
-    uint64_t k_full[kStages], v_full[kStages], k_empty[kStages], v_empty[kStages];
+    uint64_t q_full[2], q_empty[2];                       // Q buffer loaded / output stored from it
+    uint64_t k_full[kStagesK], k_empty[kStagesK];
+    uint64_t v_full[kStagesV], v_empty[kStagesV];
     uint64_t s_full, s_free;     // S(j) computed (commit) / loaded by both halves (256 arrivals)
     uint64_t p_full, pv_done;    // P(j) written by both halves (256) / P.V(j) done (commit)
+    uint64_t unit_full[2];       // unit slot published by the scheduler
+    UnitInfo unit[2];
     uint32_t tmem_base;
     int abort_flag;
 };
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kTile;
-constexpr uint32_t kOffV = kOffK + kStages * kTile;
-constexpr uint32_t kOffBar = kOffV + kStages * kTile;
+constexpr uint32_t kOffQ = 0;                                  // + kTile * buffer
+constexpr uint32_t kOffK = 2 * kTile;
+constexpr uint32_t kOffV = kOffK + kStagesK * kTile;
+constexpr uint32_t kOffBar = kOffV + kStagesV * kTile;
 constexpr size_t kSmemBytes = 1024 + kOffBar + sizeof(Smem128);
+
+// Unit u of the schedule: (batch, head) pairs in groups of kHeadGroup, inside a group the
+// query tiles from the last (longest key range under a causal mask) to the first.
+__device__ __forceinline__ UnitInfo unit_of(const AttnParams& p, int u) {
+    const int BH = p.B * p.h;
+    const int QT = p.q_pairs;
+    const int grp = u / (kHeadGroup * QT);
+    const int g_heads = min(kHeadGroup, BH - grp * kHeadGroup);
+    const int r = u - grp * kHeadGroup * QT;
+    const int qt = QT - 1 - r / g_heads;
+    const int bh = grp * kHeadGroup + r % g_heads;
+    UnitInfo x;
+    x.b = bh / p.h;
+    x.head = bh - x.b * p.h;
+    x.q0 = qt * BM;
+    int vl = p.Lk;
+    if (p.valid_lens != nullptr) vl = min(max(p.valid_lens[x.b], 0), p.Lk);
+    const bool can_skip = (p.dense == nullptr) && (vl >= 1);
+    int kend = can_skip ? vl : p.Lk;
+    if (can_skip && p.causal) kend = min(kend, x.q0 + BM);
+    x.n = (kend + BN - 1) / BN;   // >= 1
+    x.vl = vl;
+    return x;
+}
 
 __global__ void __launch_bounds__(kThreads, 1) attn_d128_kernel(const __grid_constant__ AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Smem128* sm = reinterpret_cast<Smem128*>(base + kOffBar);
     pdl_trigger();
-    pdl_wait();   // Qh, KVh and the mask parts come from earlier kernels
+    pdl_wait();   // Qh, KVh, the mask parts and the schedule counter come from earlier kernels
 
-    // (batch, head) pairs in groups of kHeadGroup, longest query tiles first
-    const int BH = p.B * p.h;
-    const int QT = p.q_pairs;   // query tiles of 128 rows
-    const int idx = static_cast<int>(blockIdx.x);
-    const int grp = idx / (kHeadGroup * QT);
-    const int g_heads = min(kHeadGroup, BH - grp * kHeadGroup);
-    const int r = idx - grp * kHeadGroup * QT;
-    const int qt = QT - 1 - r / g_heads;
-    const int bh = grp * kHeadGroup + r % g_heads;
-    MHA_DEVICE_CHECK(bh >= 0 && bh < BH && qt >= 0 && qt < QT && p.Lq >= 1 && p.Lk >= 1 && QT * BM >= p.Lq,
+    const int total = p.B * p.h * p.q_pairs;
+    MHA_DEVICE_CHECK(total >= 1 && p.Lq >= 1 && p.Lk >= 1 && p.q_pairs * BM >= p.Lq && p.sched != nullptr,
                      p.status, 0x2f1);
-    const int b = bh / p.h;
-    const int head = bh - b * p.h;
-    const int q0 = qt * BM;
-
-    int vl = p.Lk;
-    if (p.valid_lens != nullptr) vl = min(max(p.valid_lens[b], 0), p.Lk);
-    const bool can_skip = (p.dense == nullptr) && (vl >= 1);
-    int kend = can_skip ? vl : p.Lk;
-    if (can_skip && p.causal) kend = min(kend, q0 + BM);
-    const int n = (kend + BN - 1) / BN;   // >= 1
-
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int q_slab = b * p.h + head;
-    const int k_slab = b * 2 * p.h + head;
-    const int v_slab = k_slab + p.h;
 
     if (threadIdx.x == 0) {
-        mbar_init(&sm->q_full, 1);
-        for (int s = 0; s < kStages; ++s) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm->q_full[i], 1);
+            mbar_init(&sm->q_empty[i], 1);
+            mbar_init(&sm->unit_full[i], 1);
+        }
+        for (int s = 0; s < kStagesK; ++s) {
             mbar_init(&sm->k_full[s], 1);
-            mbar_init(&sm->v_full[s], 1);
             mbar_init(&sm->k_empty[s], 1);
+        }
+        for (int s = 0; s < kStagesV; ++s) {
+            mbar_init(&sm->v_full[s], 1);
             mbar_init(&sm->v_empty[s], 1);
         }
         mbar_init(&sm->s_full, 1);
@@ -139,62 +167,111 @@ __global__ void __launch_bounds__(kThreads, 1) attn_d128_kernel(const __grid_con
     if (warp >= 8) {
       regs_dec<64>();
       if (warp == 8 && lane == 0) {
-        // ------------------------------------------------ TMA producer
-        mbar_arrive_expect_tx(&sm->q_full, kTile);
-        for (int hf = 0; hf < 2; ++hf)
-            tma_load_4d(&p.q_map, &sm->q_full, base + kOffQ + hf * kHalf, 0, hf, q0, q_slab);
-        for (int j = 0; j < n; ++j) {
-            const int s = j % kStages;
-            const uint32_t ph = (j / kStages) & 1;
-            mbar_wait(&sm->k_empty[s], ph ^ 1, abort_flag, p.status, 0x401);
-            mbar_arrive_expect_tx(&sm->k_full[s], kTile);
+        // ------------------------------------------------ scheduler, Q and K loads
+        int next = atomicAdd(p.sched, 1);
+        uint32_t gk = 0;   // K tiles issued so far
+        for (int k = 0;; ++k) {
+            const int qb = k & 1;
+            // unit k - 2 has stored its output from this Q buffer (and every role has read its slot)
+            if (k >= 2) mbar_wait(&sm->q_empty[qb], ((k >> 1) - 1) & 1, abort_flag, p.status, 0x400);
+            if (next >= total || *abort_flag) {
+                sm->unit[qb].n = 0;
+                mbar_arrive(&sm->unit_full[qb]);
+                break;
+            }
+            const UnitInfo x = unit_of(p, next);
+            sm->unit[qb] = x;
+            mbar_arrive(&sm->unit_full[qb]);
+            next = atomicAdd(p.sched, 1);   // the unit after this one, fetched while this one loads
+            const int q_slab = x.b * p.h + x.head;
+            const int k_slab = x.b * 2 * p.h + x.head;
+            uint8_t* qbuf = base + kOffQ + qb * kTile;
+            mbar_arrive_expect_tx(&sm->q_full[qb], kTile);
             for (int hf = 0; hf < 2; ++hf)
-                tma_load_4d(&p.kv_map, &sm->k_full[s], base + kOffK + s * kTile + hf * kHalf, 0, hf, j * BN, k_slab);
-            mbar_wait(&sm->v_empty[s], ph ^ 1, abort_flag, p.status, 0x402);
-            mbar_arrive_expect_tx(&sm->v_full[s], kTile);
-            for (int hf = 0; hf < 2; ++hf)
-                tma_load_4d(&p.kv_map, &sm->v_full[s], base + kOffV + s * kTile + hf * kHalf, 0, hf, j * BN, v_slab);
+                tma_load_4d(&p.q_map, &sm->q_full[qb], qbuf + hf * kHalf, 0, hf, x.q0, q_slab);
+            for (int j = 0; j < x.n; ++j, ++gk) {
+                const int s = gk % kStagesK;
+                mbar_wait(&sm->k_empty[s], ((gk / kStagesK) & 1) ^ 1, abort_flag, p.status, 0x401);
+                mbar_arrive_expect_tx(&sm->k_full[s], kTile);
+                for (int hf = 0; hf < 2; ++hf)
+                    tma_load_4d(&p.kv_map, &sm->k_full[s], base + kOffK + s * kTile + hf * kHalf, 0, hf, j * BN,
+                                k_slab);
+            }
+        }
+      } else if (warp == 11 && lane == 0) {
+        // ------------------------------------------------ V loads
+        uint32_t gv = 0;
+        for (int k = 0;; ++k) {
+            const int qb = k & 1;
+            if (!mbar_wait(&sm->unit_full[qb], (k >> 1) & 1, abort_flag, p.status, 0x40c)) break;
+            const UnitInfo x = sm->unit[qb];
+            if (x.n == 0) break;
+            const int v_slab = x.b * 2 * p.h + p.h + x.head;
+            for (int j = 0; j < x.n; ++j, ++gv) {
+                const int s = gv % kStagesV;
+                mbar_wait(&sm->v_empty[s], ((gv / kStagesV) & 1) ^ 1, abort_flag, p.status, 0x402);
+                mbar_arrive_expect_tx(&sm->v_full[s], kTile);
+                for (int hf = 0; hf < 2; ++hf)
+                    tma_load_4d(&p.kv_map, &sm->v_full[s], base + kOffV + s * kTile + hf * kHalf, 0, hf, j * BN,
+                                v_slab);
+            }
         }
       } else if (warp == 9 && lane == 0) {
         // ------------------------------------------------ score MMAs: S(j) = Q K_j^T
         constexpr uint32_t idesc_s = idesc_bf16(BM, BN, false, false);
-        const uint32_t qa = smem_u32(base + kOffQ);
         const uint32_t k_addr = smem_u32(base + kOffK);
-        mbar_wait(&sm->q_full, 0, abort_flag, p.status, 0x403);
-        for (int j = 0; j < n; ++j) {
-            const int s = j % kStages;
-            mbar_wait(&sm->k_full[s], (j / kStages) & 1, abort_flag, p.status, 0x404);
-            // S is free once both halves have loaded S(j - 1)
-            if (j > 0) mbar_wait(&sm->s_free, (j - 1) & 1, abort_flag, p.status, 0x406);
-            tc_fence_after();
-            const uint32_t ka = k_addr + s * kTile;
+        uint32_t gk = 0;   // score tiles issued so far
+        for (int k = 0;; ++k) {
+            const int qb = k & 1;
+            if (!mbar_wait(&sm->unit_full[qb], (k >> 1) & 1, abort_flag, p.status, 0x40d)) break;
+            const int n = sm->unit[qb].n;
+            if (n == 0) break;
+            const uint32_t qa = smem_u32(base + kOffQ + qb * kTile);
+            mbar_wait(&sm->q_full[qb], (k >> 1) & 1, abort_flag, p.status, 0x403);
+            for (int j = 0; j < n; ++j, ++gk) {
+                const int s = gk % kStagesK;
+                mbar_wait(&sm->k_full[s], (gk / kStagesK) & 1, abort_flag, p.status, 0x404);
+                // S is free once both halves have loaded the previous score tile
+                if (gk > 0) mbar_wait(&sm->s_free, (gk - 1) & 1, abort_flag, p.status, 0x406);
+                tc_fence_after();
+                const uint32_t ka = k_addr + s * kTile;
 #pragma unroll
-            for (int k = 0; k < D / 16; ++k) {
-                const uint32_t off = (k >> 2) * kHalf + (k & 3) * 32;
-                mma_ss(tmem + kColS, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idesc_s,
-                       k > 0);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+                    mma_ss(tmem + kColS, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
+                           idesc_s, kk > 0);
+                }
+                tc_commit(&sm->s_full);
+                tc_commit(&sm->k_empty[s]);
             }
-            tc_commit(&sm->s_full);
-            tc_commit(&sm->k_empty[s]);
         }
       } else if (warp == 10 && lane == 0) {
         // ------------------------------------------------ P.V MMAs: O_h += P_h(j) V_j[keys of half h]
         constexpr uint32_t idesc_o = idesc_bf16(BM, D, false, true);
         const uint32_t v_addr = smem_u32(base + kOffV);
-        for (int j = 0; j < n; ++j) {
-            const int s = j % kStages;
-            mbar_wait(&sm->v_full[s], (j / kStages) & 1, abort_flag, p.status, 0x407);
-            mbar_wait(&sm->p_full, j & 1, abort_flag, p.status, 0x408);
-            tc_fence_after();
-            const uint32_t va = v_addr + s * kTile;
+        uint32_t gv = 0;   // P.V steps issued so far
+        for (int k = 0;; ++k) {
+            const int qb = k & 1;
+            if (!mbar_wait(&sm->unit_full[qb], (k >> 1) & 1, abort_flag, p.status, 0x40e)) break;
+            const int n = sm->unit[qb].n;
+            if (n == 0) break;
+            for (int j = 0; j < n; ++j, ++gv) {
+                const int s = gv % kStagesV;
+                mbar_wait(&sm->v_full[s], (gv / kStagesV) & 1, abort_flag, p.status, 0x407);
+                // P(j) written; for j = 0 also: the previous unit's output has been read out of O
+                mbar_wait(&sm->p_full, gv & 1, abort_flag, p.status, 0x408);
+                tc_fence_after();
+                const uint32_t va = v_addr + s * kTile;
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
+                for (int h = 0; h < 2; ++h)
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    mma_ts(tmem + kColO + h * 128, tmem + kColP + h * 32 + k * 8,
-                           sdesc_sw128(va + (4 * h + k) * 2048, kHalf, 1024), idesc_o, (j > 0 || k > 0) ? 1u : 0u);
-            tc_commit(&sm->pv_done);
-            tc_commit(&sm->v_empty[s]);
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_ts(tmem + kColO + h * 128, tmem + kColP + h * 32 + kk * 8,
+                               sdesc_sw128(va + (4 * h + kk) * 2048, kHalf, 1024), idesc_o,
+                               (j > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(&sm->pv_done);
+                tc_commit(&sm->v_empty[s]);
+            }
         }
       }
       tc_fence_before();
@@ -205,165 +282,191 @@ __global__ void __launch_bounds__(kThreads, 1) attn_d128_kernel(const __grid_con
           tc_fence_after();
           tmem_dealloc(tmem, kTmemCols);
       }
+      if (warp == 8 && lane == 0) {
+          // the last CTA to finish leaves the schedule counter at zero for the next launch
+          __threadfence();
+          if (atomicAdd(p.sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+              atomicExch(p.sched, 0);
+              atomicExch(p.sched + 1, 0);
+          }
+      }
     } else {
         regs_inc<216>();
         // ------------------------------------------------ softmax: thread (h, row), keys 64 h .. 64 h + 63
         const int h = warp >> 2;
         const int row = (warp & 3) * 32 + lane;
-        const int qi = q0 + row;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t s_tmem = tmem + lane_off + kColS + h * 64;
         const uint32_t p_tmem = tmem + lane_off + kColP + h * 32;
         const uint32_t o_tmem = tmem + lane_off + kColO + h * 128;
-        float m = -CUDART_INF_F;
-        float l = 0.0f;
-        for (int j = 0; j < n; ++j) {
-            mbar_wait(&sm->s_full, j & 1, abort_flag, p.status, 0x409);
+        uint32_t g = 0;   // score tiles consumed so far
+        for (int k = 0;; ++k) {
+            const int qb = k & 1;
+            const bool ok = mbar_wait(&sm->unit_full[qb], (k >> 1) & 1, abort_flag, p.status, 0x40f);
+            const UnitInfo x = sm->unit[qb];
             __syncwarp();
-            tc_fence_after();
-            uint32_t u[64];
-            tmem_ld_x64(s_tmem, u);
-            tc_fence_before();
-            mbar_arrive(&sm->s_free);
-            const int k0 = j * BN + h * 64;   // first key of this half
-            const bool edge = (p.dense != nullptr) || (k0 + 64 > vl) || (p.causal && k0 + 63 > q0);
-            float sc = p.scale_log2;
-            if (edge) {
-                const int lim = min(vl, p.causal ? qi + 1 : p.Lk) - k0;
-                const int oob = p.Lk - k0;
-#pragma unroll
-                for (int c = 0; c < 64; ++c) {
-                    const float x = (c < lim) ? __uint_as_float(u[c]) * sc : kMaskedLog2;   // -1e9 fill, after scaling
-                    u[c] = __float_as_uint((c < oob) ? x : -CUDART_INF_F);                   // not a key at all
-                }
-                if (p.dense != nullptr && qi < p.Lq) {
-                    const long mrow = (p.dense_mq == 1) ? 0 : qi;
-                    const long mq = (p.dense_mq == 1) ? 1 : p.Lq;
-                    const uint8_t* mr = p.dense + (static_cast<long>(b) * mq + mrow) * p.Lk + k0;
-                    uint32_t keep[2];
-#pragma unroll
-                    for (int w = 0; w < 2; ++w) {
-                        uint32_t bits = 0;
-#pragma unroll 1
-                        for (int c = 0; c < 32; ++c)
-                            if (32 * w + c >= oob || mr[32 * w + c] != 0) bits |= 1u << c;
-                        keep[w] = bits;
-                    }
-#pragma unroll
-                    for (int c = 0; c < 64; ++c)
-                        if (!((keep[c >> 5] >> (c & 31)) & 1u)) u[c] = __float_as_uint(kMaskedLog2);
-                }
-                sc = 1.0f;
-            }
-            float a4[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                float a = fmax3(__uint_as_float(u[16 * k]), __uint_as_float(u[16 * k + 1]),
-                                __uint_as_float(u[16 * k + 2]));
-#pragma unroll
-                for (int e = 3; e < 15; e += 2)
-                    a = fmax3(a, __uint_as_float(u[16 * k + e]), __uint_as_float(u[16 * k + e + 1]));
-                a4[k] = fmaxf(a, __uint_as_float(u[16 * k + 15]));
-            }
-            const float mt = fmaxf(fmax3(a4[0], a4[1], a4[2]), a4[3]);
-            const float m_new = fmaxf(m, mt * sc);
-            float alpha = 1.0f;
-            bool grow = false;
-            if (m == -CUDART_INF_F) {
-                m = m_new;   // first keys of this half (-inf while every key so far is past L_k)
-            } else {
-                grow = (m_new - m) > kRescaleThreshold;
-                if (grow) {
-                    alpha = ex2_approx(m - m_new);
-                    l *= alpha;
-                    m = m_new;
-                }
-            }
-            // with no key of this half yet (m = -inf) every weight is exp2(-inf) = 0
-            const float mref = (m == -CUDART_INF_F) ? 0.0f : m;
-            const float2 sc2 = make_float2(sc, sc);
-            const float2 nm2 = make_float2(-mref, -mref);
-            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                             make_float2(0.f, 0.f)};
-            uint32_t pk[32];
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                float2 x = ffma2(make_float2(__uint_as_float(u[2 * c]), __uint_as_float(u[2 * c + 1])), sc2, nm2);
-                x.x = ex2_approx(x.x);
-                x.y = ex2_approx(x.y);
-                acc[c & 3] = fadd2(acc[c & 3], x);
-                pk[c] = pack_bf16x2(x.x, x.y);
-            }
-            const float2 s4 = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
-            l += s4.x + s4.y;
-            if (j > 0) {
-                // P and O are busy until P.V(j - 1) has completed
-                mbar_wait(&sm->pv_done, (j - 1) & 1, abort_flag, p.status, 0x40a);
+            // every softmax thread takes the same decision (a give-up in one thread stops all)
+            if (!named_bar_and(1, 2 * BM, ok && x.n > 0)) break;
+            const int n = x.n, vl = x.vl, q0 = x.q0, b = x.b;
+            const int qi = q0 + row;
+            float m = -CUDART_INF_F;
+            float l = 0.0f;
+            for (int j = 0; j < n; ++j, ++g) {
+                mbar_wait(&sm->s_full, g & 1, abort_flag, p.status, 0x409);
                 __syncwarp();
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, grow)) {
+                uint32_t u[64];
+                tmem_ld_x64(s_tmem, u);
+                tc_fence_before();
+                mbar_arrive(&sm->s_free);
+                const int k0 = j * BN + h * 64;   // first key of this half
+                const bool edge = (p.dense != nullptr) || (k0 + 64 > vl) || (p.causal && k0 + 63 > q0);
+                float sc = p.scale_log2;
+                if (edge) {
+                    const int lim = min(vl, p.causal ? qi + 1 : p.Lk) - k0;
+                    const int oob = p.Lk - k0;
 #pragma unroll
-                    for (int q8 = 0; q8 < 8; ++q8) {
-                        uint32_t o[16];
-                        tmem_ld_x16(o_tmem + q8 * 16, o);
+                    for (int c = 0; c < 64; ++c) {
+                        const float xs = (c < lim) ? __uint_as_float(u[c]) * sc : kMaskedLog2;   // -1e9 fill, after scaling
+                        u[c] = __float_as_uint((c < oob) ? xs : -CUDART_INF_F);                  // not a key at all
+                    }
+                    if (p.dense != nullptr && qi < p.Lq) {
+                        const long mrow = (p.dense_mq == 1) ? 0 : qi;
+                        const long mq = (p.dense_mq == 1) ? 1 : p.Lq;
+                        const uint8_t* mr = p.dense + (static_cast<long>(b) * mq + mrow) * p.Lk + k0;
+                        uint32_t keep[2];
 #pragma unroll
-                        for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-                        tmem_st_x16(o_tmem + q8 * 16, o);
+                        for (int w = 0; w < 2; ++w) {
+                            uint32_t bits = 0;
+#pragma unroll 1
+                            for (int c = 0; c < 32; ++c)
+                                if (32 * w + c >= oob || mr[32 * w + c] != 0) bits |= 1u << c;
+                            keep[w] = bits;
+                        }
+#pragma unroll
+                        for (int c = 0; c < 64; ++c)
+                            if (!((keep[c >> 5] >> (c & 31)) & 1u)) u[c] = __float_as_uint(kMaskedLog2);
+                    }
+                    __syncwarp();   // rows past L_q skip the dense mask: reconverge before warp-wide instructions
+                    sc = 1.0f;
+                }
+                float a4[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float a = fmax3(__uint_as_float(u[16 * q]), __uint_as_float(u[16 * q + 1]),
+                                    __uint_as_float(u[16 * q + 2]));
+#pragma unroll
+                    for (int e = 3; e < 15; e += 2)
+                        a = fmax3(a, __uint_as_float(u[16 * q + e]), __uint_as_float(u[16 * q + e + 1]));
+                    a4[q] = fmaxf(a, __uint_as_float(u[16 * q + 15]));
+                }
+                const float mt = fmaxf(fmax3(a4[0], a4[1], a4[2]), a4[3]);
+                const float m_new = fmaxf(m, mt * sc);
+                float alpha = 1.0f;
+                bool grow = false;
+                if (m == -CUDART_INF_F) {
+                    m = m_new;   // first keys of this half (-inf while every key so far is past L_k)
+                } else {
+                    grow = (m_new - m) > kRescaleThreshold;
+                    if (grow) {
+                        alpha = ex2_approx(m - m_new);
+                        l *= alpha;
+                        m = m_new;
                     }
                 }
+                // with no key of this half yet (m = -inf) every weight is exp2(-inf) = 0
+                const float mref = (m == -CUDART_INF_F) ? 0.0f : m;
+                const float2 sc2 = make_float2(sc, sc);
+                const float2 nm2 = make_float2(-mref, -mref);
+                float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                 make_float2(0.f, 0.f)};
+                uint32_t pk[32];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    float2 e2 = ffma2(make_float2(__uint_as_float(u[2 * c]), __uint_as_float(u[2 * c + 1])), sc2, nm2);
+                    e2.x = ex2_approx(e2.x);
+                    e2.y = ex2_approx(e2.y);
+                    acc[c & 3] = fadd2(acc[c & 3], e2);
+                    pk[c] = pack_bf16x2(e2.x, e2.y);
+                }
+                const float2 s4 = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+                l += s4.x + s4.y;
+                if (j > 0) {
+                    // P and O are busy until P.V(j - 1) has completed (for j = 0 the previous
+                    // unit's output stage already waited for its last P.V)
+                    mbar_wait(&sm->pv_done, (g - 1) & 1, abort_flag, p.status, 0x40a);
+                    __syncwarp();
+                    tc_fence_after();
+                    if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll
+                        for (int q8 = 0; q8 < 8; ++q8) {
+                            uint32_t o[16];
+                            tmem_ld_x16(o_tmem + q8 * 16, o);
+#pragma unroll
+                            for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                            tmem_st_x16(o_tmem + q8 * 16, o);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int q4 = 0; q4 < 2; ++q4)
+                    tmem_st_x16_nowait(p_tmem + q4 * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16 * q4]));
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&sm->p_full);
             }
+            // ---------------- merge the halves; thread (h, row) writes output features 64 h .. 64 h + 63.
+            // The unit's Q buffer is idle (its last score MMA completed before this thread's last wait on
+            // S): it carries (m_h, l_h) of every half and row, then the bf16 output tile.
+            uint8_t* qbuf = base + kOffQ + qb * kTile;
+            float2* ml = reinterpret_cast<float2*>(qbuf);
+            ml[h * BM + row] = make_float2(m, l);
+            mbar_wait(&sm->pv_done, (g - 1) & 1, abort_flag, p.status, 0x40b);
+            __syncwarp();
+            tc_fence_after();
+            named_bar_sync(1, 2 * BM);   // both halves' statistics are in shared memory
+            const float2 s0 = ml[row], s1 = ml[BM + row];
+            const float M = fmaxf(s0.x, s1.x);
+            const float f0 = (s0.x == -CUDART_INF_F) ? 0.0f : ex2_approx(s0.x - M);
+            const float f1 = (s1.x == -CUDART_INF_F) ? 0.0f : ex2_approx(s1.x - M);
+            const float L = s0.y * f0 + s1.y * f1;
+            const float inv = 1.0f / L;
+            const float g0 = f0 * inv, g1 = f1 * inv;
+            uint32_t o0[64], o1[64];
+            tmem_ld_x64(tmem + lane_off + kColO + h * 64, o0);          // O_0, features 64 h ..
+            tmem_ld_x64(tmem + lane_off + kColO + 128 + h * 64, o1);    // O_1, features 64 h ..
+            named_bar_sync(1, 2 * BM);   // every thread has read the statistics the staging overwrites
+            const uint32_t stage = smem_u32(qbuf + h * kHalf) + row * 128;
 #pragma unroll
-            for (int q4 = 0; q4 < 2; ++q4)
-                tmem_st_x16_nowait(p_tmem + q4 * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16 * q4]));
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(&sm->p_full);
-        }
-        // ---------------- merge the halves; thread (h, row) writes output features 64 h .. 64 h + 63
-        // (m_h, l_h) of every half and row go through the K ring, idle since the last score
-        // MMA (completed before this thread's last wait on S)
-        float2* ml = reinterpret_cast<float2*>(base + kOffK);
-        ml[h * BM + row] = make_float2(m, l);
-        mbar_wait(&sm->pv_done, (n - 1) & 1, abort_flag, p.status, 0x40b);
-        __syncwarp();
-        tc_fence_after();
-        named_bar_sync(1, 2 * BM);   // both halves' statistics are in shared memory
-        const float2 s0 = ml[row], s1 = ml[BM + row];
-        const float M = fmaxf(s0.x, s1.x);
-        const float f0 = (s0.x == -CUDART_INF_F) ? 0.0f : ex2_approx(s0.x - M);
-        const float f1 = (s1.x == -CUDART_INF_F) ? 0.0f : ex2_approx(s1.x - M);
-        const float L = s0.y * f0 + s1.y * f1;
-        const float inv = 1.0f / L;
-        const float g0 = f0 * inv, g1 = f1 * inv;
-        uint32_t o0[64], o1[64];
-        tmem_ld_x64(tmem + lane_off + kColO + h * 64, o0);          // O_0, features 64 h ..
-        tmem_ld_x64(tmem + lane_off + kColO + 128 + h * 64, o1);    // O_1, features 64 h ..
-        // the Q tile is free (every S MMA completed before the last softmax): stage half h there
-        const uint32_t stage = smem_u32(base + kOffQ + h * kHalf) + row * 128;
+            for (int ch = 0; ch < 8; ++ch) {
+                uint32_t w[4];
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int c = ch * 8 + 2 * e;
-                w[e] = pack_bf16x2(__uint_as_float(o0[c]) * g0 + __uint_as_float(o1[c]) * g1,
-                                   __uint_as_float(o0[c + 1]) * g0 + __uint_as_float(o1[c + 1]) * g1);
+                for (int e = 0; e < 4; ++e) {
+                    const int c = ch * 8 + 2 * e;
+                    w[e] = pack_bf16x2(__uint_as_float(o0[c]) * g0 + __uint_as_float(o1[c]) * g1,
+                                       __uint_as_float(o0[c + 1]) * g0 + __uint_as_float(o1[c + 1]) * g1);
+                }
+                st_shared_v4(stage + ((ch ^ (row & 7)) << 4), w[0], w[1], w[2], w[3]);
             }
-            st_shared_v4(stage + ((ch ^ (row & 7)) << 4), w[0], w[1], w[2], w[3]);
+            if (h == 0 && p.stats != nullptr && qi < p.Lq) {
+                // the row's softmax statistics for p_attn: exp2(u - M) / L is the weight of any key
+                float2* st = reinterpret_cast<float2*>(p.stats) +
+                             (static_cast<long>(b * p.h + x.head) * p.Lq + qi);
+                *st = make_float2(M, L);
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(1, 2 * BM);
+            if (warp == 0 && lane == 0) {
+                if (!*abort_flag) {
+                    for (int hf = 0; hf < 2; ++hf)
+                        tma_store_3d(&p.ctx_map, qbuf + hf * kHalf, x.head * D + hf * 64, q0, b);
+                    tma_store_commit();
+                }
+                tma_store_wait_read();   // the buffer may take the Q tile of unit k + 2
+                mbar_arrive(&sm->q_empty[qb]);
+            }
         }
-        if (h == 0 && p.stats != nullptr && qi < p.Lq) {
-            // the row's softmax statistics for p_attn: exp2(u - M) / L is the weight of any key
-            float2* st = reinterpret_cast<float2*>(p.stats) + (static_cast<long>(q_slab) * p.Lq + qi);
-            *st = make_float2(M, L);
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(1, 2 * BM);
-        if (warp == 0 && lane == 0 && !*abort_flag) {
-            for (int hf = 0; hf < 2; ++hf)
-                tma_store_3d(&p.ctx_map, base + kOffQ + hf * kHalf, head * D + hf * 64, q0, b);
-            tma_store_commit();
-            tma_store_wait_all();
-        }
+        if (warp == 0 && lane == 0) tma_store_wait_all();
         tc_fence_before();
         named_bar_sync(3, kThreads);
     }
@@ -373,10 +476,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_d128_kernel(const __grid_con
 
 cudaError_t launch_attn_tc_d128(const AttnParams& p, cudaStream_t s) {
     static_assert(kSmemBytes <= 232448, "shared memory budget");
+    if (p.sched == nullptr) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(attn_d128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
-    const unsigned grid = static_cast<unsigned>(p.q_pairs) * p.B * p.h;
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const long units = static_cast<long>(p.q_pairs) * p.B * p.h;
+    const unsigned grid = static_cast<unsigned>(std::max(1L, std::min<long>(units, sms)));
     return launch_pdl(attn_d128_kernel, dim3(grid), dim3(kThreads), kSmemBytes, s, p);
 }
 

@@ -113,6 +113,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
     volatile int* abort_flag = &sm->abort_flag;
     pdl_trigger();
     pdl_wait();   // inputs, bias and residual may come from the previous kernel
+    if (p.zero_words != nullptr && blockIdx.x == 0 && threadIdx.x == 0) {
+        // after the wait: every earlier kernel on the stream (an attention launch drawing
+        // from this counter included) has completed
+        p.zero_words[0] = 0;
+        p.zero_words[1] = 0;
+    }
 
     if (warp == 0) {
         // ---------------- TMA producer

@@ -157,6 +157,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     volatile int* abort_flag = &sm->abort_flag;
     pdl_trigger();
     pdl_wait();   // inputs, bias and residual may come from the previous kernel
+    if (p.zero_words != nullptr && blockIdx.x == 0 && threadIdx.x == 0) {
+        // after the wait: every earlier kernel on the stream (an attention launch drawing
+        // from this counter included) has completed
+        p.zero_words[0] = 0;
+        p.zero_words[1] = 0;
+    }
 
     if (warp == 0) {
         // ---------------- TMA producer (both CTAs)

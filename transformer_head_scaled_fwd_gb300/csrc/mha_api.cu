@@ -43,7 +43,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // ---------------------------------------------------------------- workspace layout
 struct Layout {
-    size_t q, kv, ctx, stat, total;
+    size_t q, kv, ctx, stat, sched, total;
 };
 
 // Workspace of a bf16 problem run on the fp32 kernels: the fp32 forward's own
@@ -62,7 +62,8 @@ bool layout_of(mha_dtype_t dt, int B, int Lq, int Lk, int d, int h, Layout* L) {
     L->kv = align256(L->q + es * B * h * static_cast<size_t>(Lq) * dk);
     L->ctx = align256(L->kv + es * B * 2 * h * static_cast<size_t>(Lk) * dk);
     L->stat = align256(L->ctx + es * B * static_cast<size_t>(Lq) * d);
-    L->total = align256(L->stat + sizeof(float) * 2 * B * h * static_cast<size_t>(Lq));
+    L->sched = align256(L->stat + sizeof(float) * 2 * B * h * static_cast<size_t>(Lq));
+    L->total = L->sched + 256;   // the persistent attention's schedule counter (2 ints)
     return true;
 }
 
@@ -413,6 +414,7 @@ mha_status_t qkv_bf16_impl(const void* query, const void* key, const void* value
     p.out_plain = 0;
     p.dk_slabs = narrow ? 1 : dk / 64;
     p.narrow_shift = narrow ? (dk == 8 ? 3 : dk == 16 ? 4 : 5) : 0;
+    p.zero_words = reinterpret_cast<int*>(ws + L.sched);
     p.status = device_status_ptr();
     if (!p.status) return fail(MHA_ERR_CUDA, "device status word unavailable");
     (void)max_m;
@@ -493,6 +495,7 @@ mha_status_t attention_impl(mha_dtype_t dt, int B, int L_q, int L_k, int d_model
     const bool d128 = dk == 128;
     const int q_rows = d128 ? mha::kAttnBM : 2 * mha::kAttnBM;   // query rows per CTA
     p.q_pairs = (L_q + q_rows - 1) / q_rows;
+    p.sched = reinterpret_cast<int*>(ws + L.sched);
     p.status = device_status_ptr();
     if (!p.status) return fail(MHA_ERR_CUDA, "device status word unavailable");
     cudaError_t e = d128 ? mha::launch_attn_tc_d128(p, s) : mha::launch_attn_tc(p, s);

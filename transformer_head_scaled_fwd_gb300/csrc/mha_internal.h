@@ -47,6 +47,7 @@ struct GemmParams {
                           // out map {d_k, L, planes, B}, box {d_k, 128, 64/d_k, 1}, unswizzled
     int relu;             // 1: max(0, .) after the bias (first FFN layer)
     int* status;
+    int* zero_words;      // or nullptr: 2 ints set to zero (the attention schedule counter of the workspace)
 };
 
 // The tile bookkeeping of a GemmParams is consistent: 1 to 3 groups, K a positive
@@ -88,6 +89,7 @@ struct AttnParams {
                            // them to 64 columns, ctx_map stores d_k columns unswizzled); 0 otherwise
     float* p_attn;         // p_attn kernel only: fp32 [B, h, L_q, L_k]
     int* status;
+    int* sched;            // d_k = 128 kernel: 2 ints in the workspace (next unit, CTAs finished), zero at launch
     // p_attn kernel only: fp32 {L_k, L_q, B*h}, box {32, 128, 1} (when L_k % 4 == 0). Kept last:
     // placed first, it moved the attention kernel's own tensor maps and fields and made that
     // kernel 1.8 % slower on the long workload (0.5205 against 0.5113 ms, same box).
@@ -96,7 +98,8 @@ struct AttnParams {
 
 size_t attn_tc_smem_bytes();
 cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t s);
-// d_k = 128: same parameters with q_map / kv_map as {64, 2, L, planes} and q_pairs = ceil(L_q / 128)
+// d_k = 128: same parameters with q_map / kv_map as {64, 2, L, planes}, q_pairs = ceil(L_q / 128)
+// and sched set (persistent: one CTA per SM drawing query tiles from the counter)
 cudaError_t launch_attn_tc_d128(const AttnParams& p, cudaStream_t s);
 
 // p_attn for the bf16 path (pattn_tc.cu): the scores recomputed on the tensor cores from
