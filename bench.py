@@ -144,14 +144,27 @@ class ClockSampler:
         os.unlink(self.file.name)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        smax = [v for v in (num(r[2]) for r in rows) if v is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower() == "active"})
-        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        power = [v for v in (num(r[3]) for r in rows) if v is not None]
+        # "under load": samples drawing at least half the peak power seen (and 150 W), i.e. taken
+        # while kernels ran rather than between the timed loops
+        p_max = max(power) if power else None
+        cut = max(150.0, 0.5 * p_max) if p_max else None
+        loaded = [r for r in rows if cut is not None and num(r[3]) is not None and num(r[3]) >= cut]
+        sm_loaded = [v for v in (num(r[1]) for r in loaded) if v is not None]
+        sm_all = [v for v in (num(r[1]) for r in rows) if v is not None]
+        sm = sm_loaded or sm_all
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": reasons, "samples": len(rows),
-                "power_w_max": max(power) if power else None}
+                "reasons": reasons, "samples": len(rows), "samples_under_load": len(sm_loaded),
+                "sm_mhz_min_under_load": min(sm_loaded) if sm_loaded else None,
+                "power_w_max": p_max}
 
 
 def dist_setup():

@@ -53,3 +53,33 @@ def test_host_pipeline_launch_count_follows_the_chunk_rule():
     assert f(1, 8192, 8192, 1024, False, False) == 3 + 2        # one sequence: one chunk
     assert f(3, 4096, 4096, 1024, False, False) == 3 * 2 + 2    # 25 MB: a small call, 2 chunks
     assert f(3, 8192, 8192, 1024, False, False) == 3 * 3 + 2    # 50 MB: up to 4 chunks, B = 3 of them
+
+
+def test_clock_summary_takes_the_median_under_load(tmp_path):
+    """The clock record's sm_mhz is the median over samples drawn while kernels ran (power at
+    least half the peak seen and 150 W); idle samples between timed loops and unparsable
+    fields do not count, and every active slowdown reason is reported."""
+    import bench
+    f = tmp_path / "clocks.csv"
+    na = "Not Active"
+    f.write_text("\n".join([
+        f"0, 2070, 2070, 95.0, 0x0, {na}, {na}, {na}, {na}",           # idle
+        f"0, 2070, 2070, 820.5, 0x4, {na}, {na}, {na}, Active",        # under load, power cap
+        f"0, 1980, 2070, 900.0, 0x4, {na}, {na}, {na}, Active",
+        f"0, 1500, 2070, 120.0, 0x0, {na}, {na}, {na}, {na}",          # idle, low clock
+        f"0, [N/A], 2070, [N/A], 0x0, {na}, {na}, {na}, {na}",
+    ]) + "\n")
+
+    class _F:
+        name = str(f)
+
+        def flush(self):
+            pass
+
+    c = bench.ClockSampler(0)
+    c.proc, c.file = object(), _F()
+    s = c.summary()
+    assert s["samples"] == 5 and s["samples_under_load"] == 2
+    assert s["sm_mhz"] == 2025.0 and s["sm_mhz_min_under_load"] == 1980.0
+    assert s["sm_max_mhz"] == 2070.0 and s["power_w_max"] == 900.0
+    assert s["reasons"] == ["sw_power_cap"]
