@@ -7,39 +7,37 @@
 // Unit of work = one 128-row query tile of one (batch, head); key tiles of 128.
 //
 // Each query row is shared by two softmax threads: thread (h, row) of warpgroup h
-// takes keys 64 h .. 64 h + 63 of every key tile and keeps its own running max m_h,
-// sum l_h and output accumulator O_h = sum over its keys of p V. Softmax is exact
-// per half (the online rewrite), and the two halves merge once at the end:
-//     M = max(m_0, m_1),  f_h = 2^(m_h - M),
-//     out = (f_0 O_0 + f_1 O_1) / (f_0 l_0 + f_1 l_1),
-// which is the softmax over all keys of the row (a half whose keys are all masked
-// carries the -1e9 fill as its max, so its factor underflows to zero whenever the
-// other half has an allowed key, and a fully masked row stays uniform over L_k).
-// Two threads per row give each sub-partition two softmax warps and halve each
-// warp's chain of loads, maxima, exponentials and stores per key tile, so the
-// tensor pipe (S = Q K^T and P.V, 8 MMAs of N = 128 each per key tile) no longer
-// waits on a single warp's softmax.
+// takes keys 64 h .. 64 h + 63 of every key tile. The two halves of a row exchange
+// their tile maxima through shared memory (a named barrier per pair of warps), so
+// both keep the same reference max m (the lazy online rewrite: m moves only when the
+// row max grows by more than 2^8, exact because the final O / l uses the same m),
+// each adds its own share l_h of the row sum, writes its 64 weights into one half of
+// the tile's P and rescales its 64 features of the one output accumulator O; the row
+// ends as O / (l_0 + l_1). Two threads per row give each sub-partition two softmax
+// warps and halve each warp's chain of loads, maxima, exponentials and stores.
 //
 // Persistent: one CTA per SM draws query tiles ("units": (batch, head, 128 query rows))
 // from a counter in the workspace, in the order (groups of kHeadGroup (batch, head)
 // pairs, longest query tiles first), so the K/V in flight fit L2 and the short tiles
-// fill the end. The next unit's Q, K and V tiles are loaded, and its first score tile
+// fill the end. The next unit's Q, K and V tiles are loaded, and its first score tiles
 // computed, while the current unit's softmax and output finish: a CTA's set-up is paid
 // once, not once per query tile. The last CTA to finish resets the counter; the Q/K/V
 // projection kernel also zeroes it before the first use of a workspace.
 //
-// Tensor memory (512 columns):
-//   S    [0,128)    fp32 scores of the current key tile (released as soon as both
-//                   halves have loaded them: S(j+1) is computed during softmax(j))
-//   P    [128,192)  bf16 weights, P_0 (keys 0..63) in [128,160), P_1 in [160,192)
-//   O_0  [256,384)  fp32 output accumulator of key half 0 (128 features)
-//   O_1  [384,512)  fp32 output accumulator of key half 1
+// Tensor memory (512 columns), every tile double-buffered so that neither MMA waits
+// on the other's consumer:
+//   S_0 S_1  [0,256)    fp32 scores of key tiles j = 0, 2, ... / 1, 3, ...: S(j + 2) is
+//                       computed once both halves have loaded S(j)
+//   P_0 P_1  [256,384)  bf16 weights of those tiles (keys 0..63 in the first 32 columns,
+//                       64..127 in the next 32): the softmax writes P(j) without waiting
+//                       for P.V(j - 1), only for P.V(j - 2)
+//   O        [384,512)  fp32 output accumulator (128 features)
 // Shared memory: two Q buffers (unit u uses buffer u mod 2; after its last score MMA
-// the buffer stages the unit's output for the TMA store), a K ring of 3 stages and a
-// V ring of 2 (every tile two 64-wide 128-byte-swizzled halves). S = Q K^T is SS-MMA
-// M=128 N=128 (8 k-steps); O_h += P_h V_h takes P_h from tensor memory and the 64 value
-// rows of half h MN-major with N = 128 (the two 64-wide feature halves are the
-// descriptor's two MN blocks, LBO apart): 4 k-steps per half.
+// the buffer carries the halves' sums and stages the unit's output for the TMA store),
+// a K ring of 3 stages and a V ring of 2 (every tile two 64-wide 128-byte-swizzled
+// halves), the maxima exchange. S = Q K^T is SS-MMA M=128 N=128 (8 k-steps);
+// O += P V takes P from tensor memory and V MN-major with N = 128 (the two 64-wide
+// feature halves are the descriptor's two MN blocks, LBO apart): 8 k-steps.
 // Warps: 0-3 / 4-7 softmax of key half 0 / 1 (one thread per query row), 8 scheduler
 // and Q/K loads, 9 score MMAs (and tensor-memory allocation), 10 P.V MMAs, 11 V loads.
 // Registers: 168 per thread at launch; the third warpgroup drops to 64 and the softmax
@@ -64,9 +62,9 @@ constexpr int kThreads = 384;
 constexpr uint32_t kHalf = 128 * 128;        // one 128-row x 64-column bf16 half tile = 16 KB
 constexpr uint32_t kTile = 2 * kHalf;        // 128 x 128 bf16
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;
-constexpr uint32_t kColP = 128;              // + 32 h
-constexpr uint32_t kColO = 256;              // + 128 h
+constexpr uint32_t kColS = 0;                // + 128 b: score buffers S_0, S_1
+constexpr uint32_t kColP = 256;              // + 64 b + 32 h: weight buffers P_0, P_1 (two halves each)
+constexpr uint32_t kColO = 384;              // output accumulator, 128 features
 constexpr float kMaskedLog2 = -1.0e9f * 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;
 constexpr int kHeadGroup = 8;
@@ -80,18 +78,23 @@ struct Smem128 {
     uint64_t q_full[2], q_empty[2];                       // Q buffer loaded / output stored from it
     uint64_t k_full[kStagesK], k_empty[kStagesK];
     uint64_t v_full[kStagesV], v_empty[kStagesV];
-    uint64_t s_full, s_free;     // S(j) computed (commit) / loaded by both halves (256 arrivals)
-    uint64_t p_full, pv_done;    // P(j) written by both halves (256) / P.V(j) done (commit)
+    uint64_t s_full[2];          // score buffer b holds S(j) (commit)
+    uint64_t s_free[2];          // S(j) of buffer b loaded by both halves (256 arrivals)
+    uint64_t p_full[2];          // P(j) of weight buffer b written by both halves (256 arrivals)
+    uint64_t p_free[2];          // P.V(j) of weight buffer b done (commit): P_b free, O holds tile j
     uint64_t unit_full[2];       // unit slot published by the scheduler
     UnitInfo unit[2];
     uint32_t tmem_base;
     int abort_flag;
+    float mx[2][2][BM];          // [tile parity][half][row]: the halves' tile maxima, exchanged
 };
 constexpr uint32_t kOffQ = 0;                                  // + kTile * buffer
 constexpr uint32_t kOffK = 2 * kTile;
 constexpr uint32_t kOffV = kOffK + kStagesK * kTile;
 constexpr uint32_t kOffBar = kOffV + kStagesV * kTile;
-constexpr size_t kSmemBytes = 1024 + kOffBar + sizeof(Smem128);
+// The dynamic shared memory starts 1024-byte aligned (checked at entry): no alignment slack, which
+// leaves room for the maxima exchange beside the rings.
+constexpr size_t kSmemBytes = kOffBar + sizeof(Smem128);
 
 // Unit u of the schedule: (batch, head) pairs in groups of kHeadGroup, inside a group the
 // query tiles from the last (longest key range under a causal mask) to the first.
@@ -118,9 +121,14 @@ __device__ __forceinline__ UnitInfo unit_of(const AttnParams& p, int u) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1) attn_d128_kernel(const __grid_constant__ AttnParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* base = smem_raw;
     Smem128* sm = reinterpret_cast<Smem128*>(base + kOffBar);
+    if ((smem_u32(base) & 1023u) != 0) {
+        // the 128-byte-swizzled tiles need 1024-byte alignment: refuse rather than compute garbage
+        if (threadIdx.x == 0) atomicCAS(p.status, 0, 0x2f2);
+        return;
+    }
     pdl_trigger();
     pdl_wait();   // Qh, KVh, the mask parts and the schedule counter come from earlier kernels
 
@@ -144,10 +152,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_d128_kernel(const __grid_con
             mbar_init(&sm->v_full[s], 1);
             mbar_init(&sm->v_empty[s], 1);
         }
-        mbar_init(&sm->s_full, 1);
-        mbar_init(&sm->s_free, 2 * BM);
-        mbar_init(&sm->p_full, 2 * BM);
-        mbar_init(&sm->pv_done, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sm->s_full[b], 1);
+            mbar_init(&sm->s_free[b], 2 * BM);
+            mbar_init(&sm->p_full[b], 2 * BM);
+            mbar_init(&sm->p_free[b], 1);
+        }
         sm->abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&p.q_map);
@@ -231,22 +241,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_d128_kernel(const __grid_con
             for (int j = 0; j < n; ++j, ++gk) {
                 const int s = gk % kStagesK;
                 mbar_wait(&sm->k_full[s], (gk / kStagesK) & 1, abort_flag, p.status, 0x404);
-                // S is free once both halves have loaded the previous score tile
-                if (gk > 0) mbar_wait(&sm->s_free, (gk - 1) & 1, abort_flag, p.status, 0x406);
+                // buffer gk mod 2 is free once both halves have loaded score tile gk - 2
+                const int sb = gk & 1;
+                if (gk >= 2) mbar_wait(&sm->s_free[sb], ((gk >> 1) - 1) & 1, abort_flag, p.status, 0x406);
                 tc_fence_after();
                 const uint32_t ka = k_addr + s * kTile;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-                    mma_ss(tmem + kColS, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-                           idesc_s, kk > 0);
+                    mma_ss(tmem + kColS + sb * 128, sdesc_sw128(qa + off, 16, 1024),
+                           sdesc_sw128(ka + off, 16, 1024), idesc_s, kk > 0);
                 }
-                tc_commit(&sm->s_full);
+                tc_commit(&sm->s_full[sb]);
                 tc_commit(&sm->k_empty[s]);
             }
         }
       } else if (warp == 10 && lane == 0) {
-        // ------------------------------------------------ P.V MMAs: O_h += P_h(j) V_j[keys of half h]
+        // ------------------------------------------------ P.V MMAs: O += P(j) V_j (128 keys, both halves)
         constexpr uint32_t idesc_o = idesc_bf16(BM, D, false, true);
         const uint32_t v_addr = smem_u32(base + kOffV);
         uint32_t gv = 0;   // P.V steps issued so far
@@ -259,17 +270,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_d128_kernel(const __grid_con
                 const int s = gv % kStagesV;
                 mbar_wait(&sm->v_full[s], (gv / kStagesV) & 1, abort_flag, p.status, 0x407);
                 // P(j) written; for j = 0 also: the previous unit's output has been read out of O
-                mbar_wait(&sm->p_full, gv & 1, abort_flag, p.status, 0x408);
+                mbar_wait(&sm->p_full[gv & 1], (gv >> 1) & 1, abort_flag, p.status, 0x408);
                 tc_fence_after();
                 const uint32_t va = v_addr + s * kTile;
+                const uint32_t pa = tmem + kColP + (gv & 1) * 64;   // keys 16 kk .. 16 kk + 15: columns 8 kk ..
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_ts(tmem + kColO + h * 128, tmem + kColP + h * 32 + kk * 8,
-                               sdesc_sw128(va + (4 * h + kk) * 2048, kHalf, 1024), idesc_o,
-                               (j > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(&sm->pv_done);
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ts(tmem + kColO, pa + kk * 8, sdesc_sw128(va + kk * 2048, kHalf, 1024), idesc_o,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(&sm->p_free[gv & 1]);
                 tc_commit(&sm->v_empty[s]);
             }
         }
@@ -294,11 +303,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_d128_kernel(const __grid_con
         regs_inc<216>();
         // ------------------------------------------------ softmax: thread (h, row), keys 64 h .. 64 h + 63
         const int h = warp >> 2;
-        const int row = (warp & 3) * 32 + lane;
-        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t s_tmem = tmem + lane_off + kColS + h * 64;
-        const uint32_t p_tmem = tmem + lane_off + kColP + h * 32;
-        const uint32_t o_tmem = tmem + lane_off + kColO + h * 128;
+        const int q = warp & 3;   // lane quarter; warps q and q + 4 hold the two halves of the same rows
+        const int row = q * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+        const uint32_t s_tmem = tmem + lane_off + kColS + h * 64;   // + 128 b
+        const uint32_t p_tmem = tmem + lane_off + kColP + h * 32;   // + 64 b
+        const uint32_t o_tmem = tmem + lane_off + kColO + h * 64;   // this half's 64 output features
         uint32_t g = 0;   // score tiles consumed so far
         for (int k = 0;; ++k) {
             const int qb = k & 1;
@@ -309,16 +319,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_d128_kernel(const __grid_con
             if (!named_bar_and(1, 2 * BM, ok && x.n > 0)) break;
             const int n = x.n, vl = x.vl, q0 = x.q0, b = x.b;
             const int qi = q0 + row;
-            float m = -CUDART_INF_F;
-            float l = 0.0f;
+            float m = -CUDART_INF_F;   // the row's reference max (log2 units), common to both halves
+            float l = 0.0f;            // this half's share of the row sum
             for (int j = 0; j < n; ++j, ++g) {
-                mbar_wait(&sm->s_full, g & 1, abort_flag, p.status, 0x409);
+                const uint32_t sb = g & 1;
+                mbar_wait(&sm->s_full[sb], (g >> 1) & 1, abort_flag, p.status, 0x409);
                 __syncwarp();
                 tc_fence_after();
                 uint32_t u[64];
-                tmem_ld_x64(s_tmem, u);
+                tmem_ld_x64(s_tmem + sb * 128, u);
                 tc_fence_before();
-                mbar_arrive(&sm->s_free);
+                mbar_arrive(&sm->s_free[sb]);
                 const int k0 = j * BN + h * 64;   // first key of this half
                 const bool edge = (p.dense != nullptr) || (k0 + 64 > vl) || (p.causal && k0 + 63 > q0);
                 float sc = p.scale_log2;
@@ -352,20 +363,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_d128_kernel(const __grid_con
                 }
                 float a4[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    float a = fmax3(__uint_as_float(u[16 * q]), __uint_as_float(u[16 * q + 1]),
-                                    __uint_as_float(u[16 * q + 2]));
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    float a = fmax3(__uint_as_float(u[16 * c4]), __uint_as_float(u[16 * c4 + 1]),
+                                    __uint_as_float(u[16 * c4 + 2]));
 #pragma unroll
                     for (int e = 3; e < 15; e += 2)
-                        a = fmax3(a, __uint_as_float(u[16 * q + e]), __uint_as_float(u[16 * q + e + 1]));
-                    a4[q] = fmaxf(a, __uint_as_float(u[16 * q + 15]));
+                        a = fmax3(a, __uint_as_float(u[16 * c4 + e]), __uint_as_float(u[16 * c4 + e + 1]));
+                    a4[c4] = fmaxf(a, __uint_as_float(u[16 * c4 + 15]));
                 }
-                const float mt = fmaxf(fmax3(a4[0], a4[1], a4[2]), a4[3]);
-                const float m_new = fmaxf(m, mt * sc);
+                // this half's tile max (log2 units), exchanged with the other half of the row
+                const float mth = fmaxf(fmax3(a4[0], a4[1], a4[2]), a4[3]) * sc;
+                sm->mx[sb][h][row] = mth;
+                named_bar_sync(4 + q, 64);   // warps q and q + 4
+                const float m_new = fmaxf(m, fmaxf(mth, sm->mx[sb][h ^ 1][row]));
                 float alpha = 1.0f;
                 bool grow = false;
                 if (m == -CUDART_INF_F) {
-                    m = m_new;   // first keys of this half (-inf while every key so far is past L_k)
+                    m = m_new;   // first keys of the row (-inf while every key so far is past L_k)
                 } else {
                     grow = (m_new - m) > kRescaleThreshold;
                     if (grow) {
@@ -374,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_d128_kernel(const __grid_con
                         m = m_new;
                     }
                 }
-                // with no key of this half yet (m = -inf) every weight is exp2(-inf) = 0
+                // with no key of the row yet (m = -inf) every weight is exp2(-inf) = 0
                 const float mref = (m == -CUDART_INF_F) ? 0.0f : m;
                 const float2 sc2 = make_float2(sc, sc);
                 const float2 nm2 = make_float2(-mref, -mref);
@@ -391,51 +405,52 @@ __global__ void __launch_bounds__(kThreads, 1) attn_d128_kernel(const __grid_con
                 }
                 const float2 s4 = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
                 l += s4.x + s4.y;
-                if (j > 0) {
-                    // P and O are busy until P.V(j - 1) has completed (for j = 0 the previous
-                    // unit's output stage already waited for its last P.V)
-                    mbar_wait(&sm->pv_done, (g - 1) & 1, abort_flag, p.status, 0x40a);
+                // weight buffer sb is free once P.V(g - 2) has read it (P.V(g - 4) was waited for
+                // at tile g - 2 and P.V(g) needs this thread's weights: the phase is unambiguous)
+                if (g >= 2) {
+                    mbar_wait(&sm->p_free[sb], ((g >> 1) - 1) & 1, abort_flag, p.status, 0x40c);
                     __syncwarp();
                     tc_fence_after();
-                    if (__any_sync(0xffffffffu, grow)) {
+                }
+                if (j > 0 && __any_sync(0xffffffffu, grow)) {
+                    // O is rescaled (this half's 64 features) once P.V(g - 1) has completed; at j = 0
+                    // the first P.V overwrites O, after the previous unit's output has been read
+                    mbar_wait(&sm->p_free[(g - 1) & 1], ((g - 1) >> 1) & 1, abort_flag, p.status, 0x40a);
+                    __syncwarp();
+                    tc_fence_after();
 #pragma unroll
-                        for (int q8 = 0; q8 < 8; ++q8) {
-                            uint32_t o[16];
-                            tmem_ld_x16(o_tmem + q8 * 16, o);
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint32_t o[16];
+                        tmem_ld_x16(o_tmem + q4 * 16, o);
 #pragma unroll
-                            for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-                            tmem_st_x16(o_tmem + q8 * 16, o);
-                        }
+                        for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                        tmem_st_x16(o_tmem + q4 * 16, o);
                     }
                 }
 #pragma unroll
                 for (int q4 = 0; q4 < 2; ++q4)
-                    tmem_st_x16_nowait(p_tmem + q4 * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16 * q4]));
+                    tmem_st_x16_nowait(p_tmem + sb * 64 + q4 * 16,
+                                       *reinterpret_cast<const uint32_t(*)[16]>(&pk[16 * q4]));
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(&sm->p_full);
+                mbar_arrive(&sm->p_full[sb]);
             }
-            // ---------------- merge the halves; thread (h, row) writes output features 64 h .. 64 h + 63.
+            // ---------------- output: thread (h, row) writes features 64 h .. 64 h + 63 of O / (l_0 + l_1).
             // The unit's Q buffer is idle (its last score MMA completed before this thread's last wait on
-            // S): it carries (m_h, l_h) of every half and row, then the bf16 output tile.
+            // S): it carries l_h of every half and row, then the bf16 output tile.
             uint8_t* qbuf = base + kOffQ + qb * kTile;
-            float2* ml = reinterpret_cast<float2*>(qbuf);
-            ml[h * BM + row] = make_float2(m, l);
-            mbar_wait(&sm->pv_done, (g - 1) & 1, abort_flag, p.status, 0x40b);
+            float* lsum = reinterpret_cast<float*>(qbuf);
+            lsum[h * BM + row] = l;
+            named_bar_sync(1, 2 * BM);   // both halves' sums are in shared memory
+            const float L = lsum[row] + lsum[BM + row];
+            const float inv = 1.0f / L;
+            const uint32_t gl = g - 1;   // the unit's last tile: its P.V completes O
+            mbar_wait(&sm->p_free[gl & 1], (gl >> 1) & 1, abort_flag, p.status, 0x40b);
             __syncwarp();
             tc_fence_after();
-            named_bar_sync(1, 2 * BM);   // both halves' statistics are in shared memory
-            const float2 s0 = ml[row], s1 = ml[BM + row];
-            const float M = fmaxf(s0.x, s1.x);
-            const float f0 = (s0.x == -CUDART_INF_F) ? 0.0f : ex2_approx(s0.x - M);
-            const float f1 = (s1.x == -CUDART_INF_F) ? 0.0f : ex2_approx(s1.x - M);
-            const float L = s0.y * f0 + s1.y * f1;
-            const float inv = 1.0f / L;
-            const float g0 = f0 * inv, g1 = f1 * inv;
-            uint32_t o0[64], o1[64];
-            tmem_ld_x64(tmem + lane_off + kColO + h * 64, o0);          // O_0, features 64 h ..
-            tmem_ld_x64(tmem + lane_off + kColO + 128 + h * 64, o1);    // O_1, features 64 h ..
-            named_bar_sync(1, 2 * BM);   // every thread has read the statistics the staging overwrites
+            uint32_t o[64];
+            tmem_ld_x64(o_tmem, o);
+            named_bar_sync(1, 2 * BM);   // every thread has read the sums the staging overwrites
             const uint32_t stage = smem_u32(qbuf + h * kHalf) + row * 128;
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch) {
@@ -443,16 +458,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_d128_kernel(const __grid_con
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int c = ch * 8 + 2 * e;
-                    w[e] = pack_bf16x2(__uint_as_float(o0[c]) * g0 + __uint_as_float(o1[c]) * g1,
-                                       __uint_as_float(o0[c + 1]) * g0 + __uint_as_float(o1[c + 1]) * g1);
+                    w[e] = pack_bf16x2(__uint_as_float(o[c]) * inv, __uint_as_float(o[c + 1]) * inv);
                 }
                 st_shared_v4(stage + ((ch ^ (row & 7)) << 4), w[0], w[1], w[2], w[3]);
             }
             if (h == 0 && p.stats != nullptr && qi < p.Lq) {
-                // the row's softmax statistics for p_attn: exp2(u - M) / L is the weight of any key
+                // the row's softmax statistics for p_attn: exp2(u - m) / L is the weight of any key
                 float2* st = reinterpret_cast<float2*>(p.stats) +
                              (static_cast<long>(b * p.h + x.head) * p.Lq + qi);
-                *st = make_float2(M, L);
+                *st = make_float2(m, L);
             }
             fence_proxy_async_smem();
             named_bar_sync(1, 2 * BM);
