@@ -411,7 +411,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_tc_kernel(const __g
                     for (int c = 0; c < 128; ++c)
                         if (!((keep[c >> 5] >> (c & 31)) & 1u)) u[c] = __float_as_uint(kMaskedLog2);
                 }
-                __syncwarp();   // rows past L_q skip the dense mask: reconverge before warp-wide instructions
                 sc = 1.0f;
             }
             // row max: 8 independent 3-input max chains of depth 8, then a small tree
