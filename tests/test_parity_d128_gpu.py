@@ -99,3 +99,54 @@ def test_d128_work_counter_reset_and_reuse():
     rows = W.sample_rows(L, 48, seed=631)
     ref = run_oracle(inp, causal=True, rows=rows)
     assert_close(outs[0].double().cpu().numpy()[:, rows], ref, "bf16")
+
+
+def test_d128_cuda_graph_replays_equal_eager():
+    """The whole d_k = 128 forward captured once in a CUDA graph (the projection zeroes the
+    attention's work counter, the persistent attention leaves it at zero) and replayed three
+    times gives the eager call's output bit for bit, with more query tiles than SMs."""
+    from gpu_helpers import to_dev
+    from transformer_head_scaled_fwd_gb300 import binding
+    B, L, d, h = 4, 1200, 512, 4
+    inp = W.random_case(640, B, L, L, d, h, self_attn=True)
+    dt = torch.bfloat16
+    x = to_dev(inp.query, dt)
+    Wt = {n: to_dev(a, dt) for n, a in inp.weights.items()}
+    ws = torch.empty(binding.workspace_size(binding.MHA_BF16, B, L, L, d, h), dtype=torch.uint8, device="cuda")
+    mask = binding.make_mask(True, None, None)
+    args = (x, x, x, Wt["w_q"], Wt["b_q"], Wt["w_k"], Wt["b_k"], Wt["w_v"], Wt["b_v"], Wt["w_o"], Wt["b_o"], h)
+    eager = torch.empty(B, L, d, dtype=dt, device="cuda")
+    binding.mha_forward(*args, out=eager, workspace=ws, mask=mask)
+    torch.cuda.synchronize()
+    out = torch.zeros(B, L, d, dtype=dt, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            binding.mha_forward(*args, out=out, workspace=ws, mask=mask, stream=s)
+    for _ in range(3):
+        out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, eager)
+    assert binding.mha_check_device_status(reset=True) == 0
+    rows = W.sample_rows(L, 32, seed=641)
+    assert_close(out.double().cpu().numpy()[:, rows], run_oracle(inp, causal=True, rows=rows), "bf16")
+
+
+def test_d128_dense_mask_many_query_tiles():
+    """A dense mask with more query tiles than SMs (every key tile visited, each CTA taking
+    several units of different batch items) and a ragged L_q: sampled rows against the
+    oracle, row sums of p_attn equal one."""
+    B, Lq, Lk, d, h = 3, 1700, 900, 512, 4
+    inp = W.random_case(650, B, Lq, Lk, d, h, kv_alias=False)
+    rng = np.random.default_rng(651)
+    dense = (rng.random((B, Lq, Lk)) < 0.5).astype(np.uint8)
+    dense[2, 1699, :] = 0
+    got, gp = run_gpu(inp, dense=dense, want_p_attn=True)
+    rows = W.sample_rows(Lq, 40, seed=652)
+    ref = run_oracle(inp, dense=dense, rows=rows)
+    assert_close(got[:, rows], ref, "bf16")
+    np.testing.assert_allclose(gp.sum(-1), 1.0, atol=ROWSUM_TOL)
+    np.testing.assert_allclose(gp[2, :, 1699], 1.0 / Lk, rtol=1e-5, atol=0)
