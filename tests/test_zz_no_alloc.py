@@ -5,9 +5,10 @@ workspace argument). It runs the same kernels as mha_forward on the same inputs,
 so its output must be bit-identical to mha_forward's with a caller workspace,
 call after call, through the C ABI; one case is also held against the oracle.
 
-The cases cover the three routes whose scratch layouts differ: bf16 on the
-tensor-core kernels (d_k = 64), bf16 with d_k = 32 (fp32 copies of the inputs
-in the scratch) and fp32. Each runs twice in a row, after a different route
+The cases cover the routes whose scratch use differs: bf16 on the tensor-core
+kernels (d_k = 64; d_k = 128, whose persistent attention draws its query tiles
+from a counter in the scratch), bf16 with d_k = 32 (fp32 copies of the inputs in
+the scratch) and fp32. Each runs twice in a row, after a different route
 has left its data in the shared scratch.
 
 This file is named so that pytest collects it last."""
@@ -62,11 +63,12 @@ def _both(binding, x, w, vl, causal, h):
 
 
 CASES = [
-    # seed, B, L, d_model, h, causal, valid lens, dtype   (d_k = 64, 64, 32, 64)
+    # seed, B, L, d_model, h, causal, valid lens, dtype   (d_k = 64, 64, 32, 64, 128)
     (201, 4, 256, 512, 8, True, [256, 200, 17, 1], "bf16"),
     (202, 3, 320, 1024, 16, False, [320, 0, 150], "bf16"),
     (203, 2, 200, 512, 16, True, [200, 93], "bf16"),
     (204, 2, 96, 256, 4, False, [96, 40], "f32"),
+    (205, 3, 700, 512, 4, True, [700, 333, 1], "bf16"),
 ]
 
 
