@@ -320,38 +320,25 @@ mha_status_t mha_qkv_projection(mha_dtype_t dt, const void* query, const void* k
         const void* A[3] = {query, key, value};
         const void* W[3] = {w_q, w_k, w_v};
         const void* bias[3] = {b_q, b_k, b_v};
-        // Q -> Qh (its own [B, h, Lq, dk]); K, V -> KVh [B, 2h, Lk, dk] -- one launch, two layouts:
-        // the Q group writes with slabs = h, so it runs as a separate launch.
+        // one launch, three groups: Q -> Qh [B, h, L_q, dk]; K, V -> planes 0..h-1 and h..2h-1
+        // of KVh [B, 2h, L_k, dk]
         for (int g = 0; g < 3; ++g) {
             p.g[g].A = static_cast<const float*>(A[g]);
             p.g[g].W = static_cast<const float*>(W[g]);
             p.g[g].bias = static_cast<const float*>(bias[g]);
+            p.g[g].out = reinterpret_cast<float*>(ws + (g == 0 ? L.q : L.kv));
+            p.g[g].L = g == 0 ? L_q : L_k;
+            p.g[g].out_j0 = g == 2 ? h : 0;
+            p.g[g].slabs = g == 0 ? h : 2 * h;
         }
+        p.ngroups = 3;
         p.B = B;
         p.K = d_model;
         p.N = d_model;
         p.dk = dk;
         p.out_plain = 0;
-        mha::F32GemmParams pq = p;
-        pq.ngroups = 1;
-        pq.slabs = h;
-        pq.g[0].out = reinterpret_cast<float*>(ws + L.q);
-        pq.g[0].L = L_q;
-        pq.g[0].out_j0 = 0;
-        cudaError_t e = mha::launch_gemm_f32(pq, s);
-        if (e != cudaSuccess) return cuda_fail(e, "Q projection launch");
-        mha::F32GemmParams pkv = p;
-        pkv.ngroups = 2;
-        pkv.slabs = 2 * h;
-        pkv.g[0] = p.g[1];
-        pkv.g[1] = p.g[2];
-        for (int g = 0; g < 2; ++g) {
-            pkv.g[g].out = reinterpret_cast<float*>(ws + L.kv);
-            pkv.g[g].L = L_k;
-            pkv.g[g].out_j0 = g * h;
-        }
-        e = mha::launch_gemm_f32(pkv, s);
-        if (e != cudaSuccess) return cuda_fail(e, "K/V projection launch");
+        cudaError_t e = mha::launch_gemm_f32(p, s);
+        if (e != cudaSuccess) return cuda_fail(e, "Q/K/V projection launch");
         return MHA_OK;
     }
 
@@ -526,7 +513,7 @@ mha_status_t output_projection_impl(mha_dtype_t dt, const void* w_o, const void*
     if (dt == MHA_F32) {
         mha::F32GemmParams p{};
         p.ngroups = 1;
-        p.B = B; p.K = d_model; p.N = d_model; p.dk = d_model / h; p.slabs = 1; p.out_plain = 1;
+        p.B = B; p.K = d_model; p.N = d_model; p.dk = d_model / h; p.g[0].slabs = 1; p.out_plain = 1;
         p.g[0].A = reinterpret_cast<const float*>(ws + L.ctx);
         p.g[0].W = static_cast<const float*>(w_o);
         p.g[0].bias = static_cast<const float*>(b_o);
@@ -896,7 +883,7 @@ mha_status_t mha_ffn_forward(mha_dtype_t dt, const void* x, const void* w_1, con
     if (dt == MHA_F32) {
         mha::F32GemmParams p{};
         p.ngroups = 1;
-        p.B = B; p.dk = 1; p.slabs = 1; p.out_plain = 1;
+        p.B = B; p.dk = 1; p.out_plain = 1;
         p.g[0].L = L;
         // layer 1: hidden = relu(x W_1^T + b_1)
         p.K = d_model; p.N = d_ff; p.relu = 1;

@@ -121,13 +121,13 @@ struct F32GemmGroup {
     float* out;          // head-split [B, slabs, L, dk] or plain [B, L, N]
     int L;
     int out_j0;
+    int slabs;           // head-split output: slabs per batch item of this group's tensor
 };
 struct F32GemmParams {
     F32GemmGroup g[3];
     int ngroups;
     int B, K, N;
     int dk;
-    int slabs;           // slabs per batch item in a head-split output
     int out_plain;
     int relu;            // 1: max(0, .) after the bias
 };

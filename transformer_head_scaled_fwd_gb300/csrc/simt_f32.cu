@@ -12,10 +12,15 @@
 //                    -1e9), softmax over keys, P.V; one warp per query row,
 //                    two passes over the keys (row max and sum, then weights);
 //                    writes the head's slab of the concatenated context and,
-//                    if asked, p_attn.
+//                    if asked, p_attn. attn_f32_short_kernel does the same for
+//                    L_k <= 64 from K and V staged in shared memory.
+// Every kernel is launched with programmatic dependent launch (launch.h) and waits
+// for the previous kernel's results before its first read of them.
 #include <math_constants.h>
 
+#include "launch.h"
 #include "mha_internal.h"
+#include "ptx.cuh"
 
 namespace mha {
 namespace {
@@ -23,6 +28,8 @@ namespace {
 constexpr int kTM = 64, kTN = 64, kTK = 16;   // block tile; 256 threads x (4 x 4) outputs
 
 __global__ void __launch_bounds__(256) gemm_f32_kernel(const __grid_constant__ F32GemmParams p) {
+    pdl_trigger();
+    pdl_wait();   // the inputs may come from the previous kernel
     const F32GemmGroup& G = p.g[blockIdx.z];
     const long M = static_cast<long>(p.B) * G.L;
     const long m0 = static_cast<long>(blockIdx.y) * kTM;
@@ -74,7 +81,7 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(const __grid_constant__ F
             } else {
                 const int slab = G.out_j0 + n / p.dk;
                 const int c = n % p.dk;
-                G.out[((b * p.slabs + slab) * G.L + l) * p.dk + c] = y;
+                G.out[((b * G.slabs + slab) * G.L + l) * p.dk + c] = y;
             }
         }
     }
@@ -82,11 +89,14 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(const __grid_constant__ F
 
 // Few rows (M = B * L <= kSmallM, e.g. the tiny workload's 20 tokens): the tiled kernel
 // above would run a handful of CTAs through a long chain of dependent k-steps. Here one
-// warp owns one output feature n of one group and all rows: its lanes stream the weight
-// row and the input rows (consecutive k per lane, so every load is coalesced) four rows
-// at a time, and a butterfly reduction finishes each dot product.
+// warp owns one output feature n of one group and all rows: the CTA stages up to 16 input
+// rows in shared memory with coalesced 16-byte loads, each warp keeps its weight row in
+// registers (lane l holds k = l, l + 32, ...) and forms the 16 dot products from shared
+// memory, and a butterfly reduction finishes each of them.
 constexpr int kSmallM = 64;
 constexpr int kSmallWarps = 8;
+constexpr int kSmallRows = 16;   // rows per pass
+constexpr int kSmallMaxK = 1024; // weight row held in registers: K / 32 <= 32 values per lane
 
 __device__ __forceinline__ float warp_sum_f32(float v) {
 #pragma unroll
@@ -94,31 +104,37 @@ __device__ __forceinline__ float warp_sum_f32(float v) {
     return v;
 }
 
-constexpr int kSmallRows = 16;   // rows accumulated per pass
-
+template <int KW>   // K / 32: weight values per lane
 __global__ void __launch_bounds__(32 * kSmallWarps) gemm_f32_small_m_kernel(const __grid_constant__ F32GemmParams p) {
+    extern __shared__ float4 xs4[];   // kSmallRows x K fp32
+    float* xs = reinterpret_cast<float*>(xs4);
+    pdl_trigger();
+    pdl_wait();   // the inputs may come from the previous kernel
     const F32GemmGroup& G = p.g[blockIdx.y];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n = blockIdx.x * kSmallWarps + warp;
-    if (n >= p.N) return;   // whole warp
-    const int K = p.K;
+    constexpr int K = KW * 32;
     const long M = static_cast<long>(p.B) * G.L;
-    const float* __restrict__ A = G.A;
-    const float* __restrict__ w = G.W + static_cast<long>(n) * K;
-    const float bias = G.bias ? G.bias[n] : 0.0f;
+    float w[KW];
+#pragma unroll
+    for (int i = 0; i < KW; ++i) w[i] = n < p.N ? __ldg(G.W + static_cast<long>(n) * K + i * 32 + lane) : 0.0f;
+    const float bias = (G.bias != nullptr && n < p.N) ? G.bias[n] : 0.0f;
     for (long m0 = 0; m0 < M; m0 += kSmallRows) {
+        const int rows = static_cast<int>(min(static_cast<long>(kSmallRows), M - m0));
+        __syncthreads();   // the previous pass has finished reading xs
+        const float4* a4 = reinterpret_cast<const float4*>(G.A + m0 * K);
+        for (int e = threadIdx.x; e < rows * K / 4; e += 32 * kSmallWarps) xs4[e] = __ldg(a4 + e);
+        __syncthreads();
+        if (n >= p.N) continue;   // whole warp; still takes part in the barriers
         float acc[kSmallRows];
 #pragma unroll
-        for (int r = 0; r < kSmallRows; ++r) acc[r] = 0.f;
-        // unrolled so that the loads of several k-steps are in flight together
-        const int rows = static_cast<int>(min(static_cast<long>(kSmallRows), M - m0));
-        const float* __restrict__ a0 = A + m0 * K;
-#pragma unroll 4
-        for (int k = lane; k < K; k += 32) {
-            const float wk = __ldg(w + k);
+        for (int r = 0; r < kSmallRows; ++r) {
+            float a = 0.0f;
+            if (r < rows) {
 #pragma unroll
-            for (int r = 0; r < kSmallRows; ++r)
-                if (r < rows) acc[r] = fmaf(__ldg(a0 + static_cast<long>(r) * K + k), wk, acc[r]);
+                for (int i = 0; i < KW; ++i) a = fmaf(xs[r * K + i * 32 + lane], w[i], a);
+            }
+            acc[r] = a;
         }
 #pragma unroll
         for (int r = 0; r < kSmallRows; ++r) acc[r] = warp_sum_f32(acc[r]);
@@ -126,7 +142,7 @@ __global__ void __launch_bounds__(32 * kSmallWarps) gemm_f32_small_m_kernel(cons
 #pragma unroll
         for (int r = 0; r < kSmallRows; ++r)
             if (lane == r) mine = acc[r];
-        if (lane < kSmallRows && m0 + lane < M) {
+        if (lane < rows) {
             const long m = m0 + lane;
             float y = mine + bias;
             if (p.relu) y = fmaxf(y, 0.0f);
@@ -136,7 +152,7 @@ __global__ void __launch_bounds__(32 * kSmallWarps) gemm_f32_small_m_kernel(cons
             } else {
                 const long b = m / G.L, l = m - b * G.L;
                 const int slab = G.out_j0 + n / p.dk;
-                G.out[((b * p.slabs + slab) * G.L + l) * p.dk + n % p.dk] = y;
+                G.out[((b * G.slabs + slab) * G.L + l) * p.dk + n % p.dk] = y;
             }
         }
     }
@@ -158,6 +174,8 @@ __device__ __forceinline__ bool allowed_f32(const F32AttnParams& p, int b, int q
 
 __global__ void __launch_bounds__(32 * kRowsPerBlock) attn_f32_kernel(const __grid_constant__ F32AttnParams p) {
     __shared__ float qs[kRowsPerBlock][kMaxDk];
+    pdl_trigger();
+    pdl_wait();   // Qh and KVh come from the projection kernel
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bh = blockIdx.y;
     const int b = bh / p.h, head = bh % p.h;
@@ -229,26 +247,133 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock) attn_f32_kernel(const __gr
     }
 }
 
+// Short key ranges (L_k <= 64, K and V of the head fit in shared memory): the CTA stages
+// K^T and V of its (batch, head) once; each warp takes one query row with one score per
+// lane (keys lane and lane + 32) computed from shared memory, the row's max and sum by
+// warp shuffles, and P.V with the lanes owning output features.
+constexpr int kShortLk = 64;
+
+__global__ void __launch_bounds__(32 * kRowsPerBlock) attn_f32_short_kernel(const __grid_constant__ F32AttnParams p) {
+    extern __shared__ float sh[];   // Kt [dk][kShortLk], V [L_k][dk], q [kRowsPerBlock][dk]
+    pdl_trigger();
+    pdl_wait();   // Qh and KVh come from the projection kernel
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.y;
+    const int b = bh / p.h, head = bh % p.h;
+    const int dk = p.dk, Lk = p.Lk;
+    float* Kt = sh;
+    float* Vs = sh + dk * kShortLk;
+    float* qs = Vs + Lk * dk;
+    const float* K = p.kv + (static_cast<long>(b) * 2 * p.h + head) * Lk * dk;
+    const float* V = p.kv + (static_cast<long>(b) * 2 * p.h + p.h + head) * Lk * dk;
+    for (int e = threadIdx.x; e < Lk * dk; e += blockDim.x) {
+        const int j = e / dk, c = e - j * dk;
+        Kt[c * kShortLk + j] = K[e];
+        Vs[e] = V[e];
+    }
+    const int qi = blockIdx.x * kRowsPerBlock + warp;
+    if (qi < p.Lq) {
+        const float* q = p.q + (static_cast<long>(bh) * p.Lq + qi) * dk;
+        for (int c = lane; c < dk; c += 32) qs[warp * dk + c] = q[c];
+    }
+    __syncthreads();
+    if (qi >= p.Lq) return;   // no barrier below
+    int vl = Lk;
+    if (p.valid_lens != nullptr) vl = min(max(p.valid_lens[b], 0), Lk);
+    const float sqrt_dk = sqrtf(static_cast<float>(dk));
+    float s[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int kj = lane + 32 * t;
+        s[t] = -CUDART_INF_F;   // not a key
+        if (kj < Lk) {
+            float dot = 0.0f;
+            for (int c = 0; c < dk; ++c) dot = fmaf(qs[warp * dk + c], Kt[c * kShortLk + kj], dot);
+            const float sc = dot / sqrt_dk;
+            s[t] = allowed_f32(p, b, qi, kj, vl) ? sc : -1.0e9f;   // fill after scaling
+        }
+    }
+    float m = fmaxf(s[0], s[1]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    float e[2], z = 0.0f;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        e[t] = (lane + 32 * t < Lk) ? expf(s[t] - m) : 0.0f;
+        z += e[t];
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+    float w[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        w[t] = e[t] / z;
+        const int kj = lane + 32 * t;
+        if (p.p_attn != nullptr && kj < Lk) p.p_attn[(static_cast<long>(bh) * p.Lq + qi) * Lk + kj] = w[t];
+    }
+    float o[kMaxDk / 32];
+#pragma unroll
+    for (int i = 0; i < kMaxDk / 32; ++i) o[i] = 0.0f;
+    for (int kj = 0; kj < Lk; ++kj) {
+        const float wt = __shfl_sync(0xffffffffu, kj < 32 ? w[0] : w[1], kj & 31);
+#pragma unroll
+        for (int i = 0; i < kMaxDk / 32; ++i) {
+            const int c = lane + 32 * i;
+            if (c < dk) o[i] = fmaf(wt, Vs[kj * dk + c], o[i]);
+        }
+    }
+    float* out = p.ctx + (static_cast<long>(b) * p.Lq + qi) * (static_cast<long>(p.h) * dk) + head * dk;
+#pragma unroll
+    for (int i = 0; i < kMaxDk / 32; ++i) {
+        const int c = lane + 32 * i;
+        if (c < dk) out[c] = o[i];
+    }
+}
+
 }  // namespace
+
+template <int KW>
+cudaError_t launch_small(const F32GemmParams& p, cudaStream_t s) {
+    const size_t smem = static_cast<size_t>(kSmallRows) * KW * 32 * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(gemm_f32_small_m_kernel<KW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    dim3 grid((p.N + kSmallWarps - 1) / kSmallWarps, p.ngroups);
+    return launch_pdl(gemm_f32_small_m_kernel<KW>, grid, dim3(32 * kSmallWarps), smem, s, p);
+}
 
 cudaError_t launch_gemm_f32(const F32GemmParams& p, cudaStream_t s) {
     int maxL = 0;
-    for (int g = 0; g < p.ngroups; ++g) maxL = max(maxL, p.g[g].L);
+    bool aligned = true;   // the small-M kernel reads its input rows as float4
+    for (int g = 0; g < p.ngroups; ++g) {
+        maxL = max(maxL, p.g[g].L);
+        aligned = aligned && (reinterpret_cast<uintptr_t>(p.g[g].A) & 15u) == 0;
+    }
     const long M = static_cast<long>(p.B) * maxL;
-    if (M <= kSmallM) {
-        dim3 grid((p.N + kSmallWarps - 1) / kSmallWarps, p.ngroups);
-        gemm_f32_small_m_kernel<<<grid, 32 * kSmallWarps, 0, s>>>(p);
-        return cudaGetLastError();
+    if (M <= kSmallM && aligned && p.K % 32 == 0 && p.K <= kSmallMaxK) {
+        switch (p.K / 32) {
+            case 8: return launch_small<8>(p, s);
+            case 16: return launch_small<16>(p, s);
+            case 24: return launch_small<24>(p, s);
+            case 32: return launch_small<32>(p, s);
+            default: break;
+        }
     }
     dim3 grid((p.N + kTN - 1) / kTN, static_cast<unsigned>((M + kTM - 1) / kTM), p.ngroups);
-    gemm_f32_kernel<<<grid, 256, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(gemm_f32_kernel, grid, dim3(256), 0, s, p);
 }
 
 cudaError_t launch_attn_f32(const F32AttnParams& p, cudaStream_t s) {
     dim3 grid((p.Lq + kRowsPerBlock - 1) / kRowsPerBlock, p.B * p.h);
-    attn_f32_kernel<<<grid, 32 * kRowsPerBlock, 0, s>>>(p);
-    return cudaGetLastError();
+    if (p.Lk <= kShortLk && p.dk <= kMaxDk) {
+        const size_t smem = sizeof(float) * (static_cast<size_t>(p.dk) * kShortLk + static_cast<size_t>(p.Lk) * p.dk +
+                                             static_cast<size_t>(kRowsPerBlock) * p.dk);
+        cudaError_t e = cudaFuncSetAttribute(attn_f32_short_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        return launch_pdl(attn_f32_short_kernel, grid, dim3(32 * kRowsPerBlock), smem, s, p);
+    }
+    return launch_pdl(attn_f32_kernel, grid, dim3(32 * kRowsPerBlock), 0, s, p);
 }
 
 }  // namespace mha
