@@ -323,9 +323,9 @@ class WorkloadRun:
         self.proj, self.attn = algorithmic_flops(self.B, self.Lq, self.Lk, self.d, self.h, wl.causal,
                                                  inp.valid_lens)
         self.flops = self.proj + self.attn
-        # launches of one mha_forward: bf16 runs three kernels; fp32 runs the Q and the K/V
-        # projections as two launches, then the attention and the output projection
-        self.launches_per_step = 3 if wl.dtype == "bf16" else 4
+        # launches of one mha_forward: the Q/K/V projection, the attention, the output projection
+        # (bf16 and fp32 alike)
+        self.launches_per_step = 3
         # attention-core algorithmic bytes: Q, K, V read once, ctx written
         es = 2 if wl.dtype == "bf16" else 4
         self.core_bytes = es * (self.B * self.Lq * self.d + 2 * self.B * self.Lk * self.d + self.B * self.Lq * self.d)
