@@ -11,8 +11,8 @@
 // for the epilogue's shared-memory staging and TMA stores.
 //
 // Warp roles (192 threads per CTA, one CTA per SM, persistent over tile pairs):
-//   warp 0     TMA producer (both CTAs): x rows and the W half into a 6-stage ring;
-//              each CTA's loads complete on its own "full" barrier.
+//   warp 0     TMA producer (both CTAs): x rows and the W half into a 3-stage ring of
+//              two k-blocks per stage; each CTA's loads complete on its own "full" barrier.
 //   warp 1     both CTAs allocate 512 tensor-memory columns together. Leader CTA
 //              (rank 0): one thread issues the MMAs and multicasts its commits to
 //              both CTAs' "empty" and "acc_full" barriers. Peer CTA (rank 1): one
@@ -32,10 +32,14 @@ namespace mha {
 namespace {
 
 constexpr int BN = kGemmBN;                                     // 256 columns per pair tile
-constexpr int kStages = 6;
+// A ring stage holds two 64-wide k-blocks ([x | W half] twice): one full/empty
+// barrier round trip (and one relay arrival) per 128 of K instead of per 64.
+constexpr int kKbPerStage = 2;
+constexpr int kStages = 3;
 constexpr uint32_t kTileABytes = kGemmBM * kGemmBK * 2;         // 16 KB: 128 rows of x
 constexpr uint32_t kHalfBBytes = (BN / 2) * kGemmBK * 2;        // 16 KB: 128 rows of W
-constexpr uint32_t kStageBytes = kTileABytes + kHalfBBytes;
+constexpr uint32_t kKbBytes = kTileABytes + kHalfBBytes;
+constexpr uint32_t kStageBytes = kKbPerStage * kKbBytes;
 constexpr uint32_t kSlabBytes = kGemmBM * 128;                  // 128 rows x 64 bf16
 constexpr uint32_t kTmemCols = 512;
 
@@ -170,14 +174,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             int it = 0;   // ring position across tiles
             for (int u = cid; u < total; u += ncl) {
                 const PairCoord c = pair_coord(p, u, n_tiles, rank, shared_rows);
-                for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                for (int kb = 0; kb < kblocks; kb += kKbPerStage, ++it) {
                     const int s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1;
+                    const int nk = min(kKbPerStage, kblocks - kb);   // 1 for the last stage of an odd count
                     mbar_wait(&sm->empty[s], ph ^ 1, abort_flag, p.status, 0x111);
                     uint8_t* a_dst = base + s * kStageBytes;
-                    mbar_arrive_expect_tx(&sm->full[s], kStageBytes);
-                    tma_load_3d(&p.a[c.grp], &sm->full[s], a_dst, kb * kGemmBK, c.l0, c.b);
-                    tma_load_2d(&p.w[c.grp], &sm->full[s], a_dst + kTileABytes, kb * kGemmBK, c.n0 + rank * (BN / 2));
+                    mbar_arrive_expect_tx(&sm->full[s], nk * kKbBytes);
+                    for (int q = 0; q < nk; ++q) {
+                        tma_load_3d(&p.a[c.grp], &sm->full[s], a_dst + q * kKbBytes, (kb + q) * kGemmBK, c.l0, c.b);
+                        tma_load_2d(&p.w[c.grp], &sm->full[s], a_dst + q * kKbBytes + kTileABytes, (kb + q) * kGemmBK,
+                                    c.n0 + rank * (BN / 2));
+                    }
                 }
             }
             // the leader's last commits into this CTA's ring have landed
@@ -194,17 +202,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                 const uint32_t d = tmem + acc * BN;
                 mbar_wait(&sm->acc_empty[acc], ((use >> 1) & 1) ^ 1, abort_flag, p.status, 0x114);
                 tc_fence_after();
-                for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                for (int kb = 0; kb < kblocks; kb += kKbPerStage, ++it) {
                     const int s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1;
+                    const int nk = min(kKbPerStage, kblocks - kb);
                     mbar_wait(&sm->full[s], ph, abort_flag, p.status, 0x112);
                     tc_fence_after();
-                    const uint32_t a_addr = smem_u32(base + s * kStageBytes);
-                    const uint32_t b_addr = a_addr + kTileABytes;
+                    for (int q = 0; q < nk; ++q) {
+                        const uint32_t a_addr = smem_u32(base + s * kStageBytes + q * kKbBytes);
+                        const uint32_t b_addr = a_addr + kTileABytes;
 #pragma unroll
-                    for (int k = 0; k < kGemmBK / 16; ++k)
-                        mma_ss_pair(d, sdesc_sw128(a_addr + k * 32, 16, 1024), sdesc_sw128(b_addr + k * 32, 16, 1024),
-                                    idesc, (kb | k) != 0);
+                        for (int k = 0; k < kGemmBK / 16; ++k)
+                            mma_ss_pair(d, sdesc_sw128(a_addr + k * 32, 16, 1024),
+                                        sdesc_sw128(b_addr + k * 32, 16, 1024), idesc, ((kb + q) | k) != 0);
+                    }
                     tc_commit_pair(&sm->empty[s], 0x3);
                 }
                 tc_commit_pair(&sm->acc_full[acc], 0x3);
@@ -215,7 +226,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             for (int s = 0; s < kStages; ++s) leader_full[s] = mapa_shared(smem_u32(&sm->full[s]), 0);
             int it = 0;
             for (int u = cid; u < total; u += ncl)
-                for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                for (int kb = 0; kb < kblocks; kb += kKbPerStage, ++it) {
                     const int s = it % kStages;
                     mbar_wait(&sm->full[s], (it / kStages) & 1, abort_flag, p.status, 0x116);
                     mbar_arrive_remote(leader_full[s]);
