@@ -59,6 +59,16 @@ def test_ffn_bf16_bench_size_sampled_rows(bnd):
     _check(got[:, rows], ref, 1.5e-2, 2e-2)
 
 
+def test_ffn_bf16_odd_k_block_counts(bnd):
+    """d_model 1344 (21 k-blocks) and d_ff 2752 (43): both layers run on pairs of SMs at B=4, L=1024,
+    each tile ending on a ring stage that holds one k-block."""
+    inp = W.make_ffn_inputs(4, 1024, 1344, 2752, seed=13)
+    got = _run(bnd, inp)
+    rows = W.sample_rows(1024, 64, seed=14)
+    ref = oracle.ffn_forward(inp.x[:, rows], inp.w_1, inp.b_1, inp.w_2, inp.b_2)
+    _check(got[:, rows], ref, 1.5e-2, 2e-2)
+
+
 @pytest.mark.parametrize("B,L,d,d_ff", [(2, 37, 48, 100), (1, 5, 512, 2048)])
 def test_ffn_fp32_matches_oracle(bnd, B, L, d, d_ff):
     inp = W.make_ffn_inputs(B, L, d, d_ff, seed=7 + d, dtype="f32")

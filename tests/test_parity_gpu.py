@@ -108,6 +108,18 @@ def test_widest_model_dimension():
     assert_close(got, ref, "bf16")
 
 
+def test_pair_gemm_odd_k_block_count():
+    """d_model 1344 = 21 k-blocks of 64 with 21 heads: at B=4, L=1024 both projections run on pairs of
+    SMs (288 and 96 tile pairs), whose ring stages hold two k-blocks, so the last stage of every tile
+    holds one; a ragged last column tile (1344 = 5.25 x 256) and ragged valid lengths."""
+    inp = W.random_case(74, 4, 1024, 1024, 1344, 21, self_attn=True, bias_scale=0.05)
+    vl = [1024, 1000, 513, 77]
+    rows = W.sample_rows(1024, 48, seed=74)
+    got, _ = run_gpu(inp, causal=True, valid_lens=vl)
+    ref = run_oracle(inp, causal=True, valid_lens=vl, rows=rows)
+    assert_close(got[:, rows], ref, "bf16")
+
+
 # ------------------------------------------------------------------ edge cases (bf16)
 def test_ragged_cross_attention_distinct_kv_bias_p_attn():
     inp = W.random_case(1, 3, 200, 77, 512, 8, kv_alias=False, bias_scale=0.1)
