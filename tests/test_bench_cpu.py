@@ -83,3 +83,14 @@ def test_clock_summary_takes_the_median_under_load(tmp_path):
     assert s["sm_mhz"] == 2025.0 and s["sm_mhz_min_under_load"] == 1980.0
     assert s["sm_max_mhz"] == 2070.0 and s["power_w_max"] == 900.0
     assert s["reasons"] == ["sw_power_cap"]
+
+
+@pytest.mark.parametrize("workload", [bench.WORKLOAD, "long_d128"])
+def test_committed_attention_profile_matches_the_sources(workload):
+    """The bench reports the attention kernel's DRAM traffic from the committed ncu summary only while
+    the kernel's sources (the kernel file and the shared headers) hash to the digest that summary was
+    taken on; a source change without a new capture would turn the figure into null."""
+    digest = bench.source_digest("attention_core", workload)
+    traffic = bench.committed_traffic("attention_core", workload)
+    assert traffic is not None, f"no committed profile for source digest {digest} ({workload})"
+    assert traffic > 0
