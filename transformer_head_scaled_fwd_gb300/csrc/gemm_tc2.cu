@@ -115,6 +115,10 @@ __device__ __forceinline__ int pair_units(const GemmParams& p, int n_tiles) {
     return total;
 }
 
+// kRes: the instance for launches with a residual (the sublayer's W_o): each slab's residual
+// values are requested one slab ahead, like the bias, so their load latency stays off the
+// epilogue's path; launches without one keep the lighter epilogue.
+template <bool kRes>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_tc2_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -255,6 +259,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             // slab's while the current one is converted: its load latency stays hidden
             uint4 bias_cur[8];
             load_bias_slab(G.bias, c.n0, p.N, bias_cur);
+            // this thread's output row of the residual (nullptr: none, or a row past L)
+            const __nv_bfloat16* res_row =
+                (kRes && G.residual != nullptr && c.l0 + row < G.L)
+                    ? G.residual + (static_cast<long>(c.b) * G.L + c.l0 + row) * p.N
+                    : nullptr;
+            uint4 res_cur[8];
+            if constexpr (kRes) load_residual_slab(res_row, c.n0, p.N, res_cur);
             mbar_wait(&sm->acc_full[acc], (use >> 1) & 1, abort_flag, p.status, 0x113);
             __syncwarp();
             tc_fence_after();
@@ -264,6 +275,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                 const int n = c.n0 + slab * 64;
                 uint4 bias_next[8];
                 load_bias_slab(G.bias, slab + 1 < BN / 64 ? n + 64 : p.N, p.N, bias_next);
+                uint4 res_next[8];
+                if constexpr (kRes) load_residual_slab(res_row, slab + 1 < BN / 64 ? n + 64 : p.N, p.N, res_next);
                 uint32_t v[64];
                 tmem_ld_x64(t_row + slab * 64, v);
                 if (slab == BN / 64 - 1) {
@@ -279,7 +292,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                 }
                 if (n >= p.N) {   // uniform across the CTA
 #pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) bias_cur[ch] = bias_next[ch];
+                    for (int ch = 0; ch < 8; ++ch) {
+                        bias_cur[ch] = bias_next[ch];
+                        if constexpr (kRes) res_cur[ch] = res_next[ch];
+                    }
                     continue;
                 }
                 const int sb = slabs_issued & 1;
@@ -289,15 +305,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                 const uint32_t sbuf = smem_u32(base + kOffStage + sb * kSlabBytes);
                 const uint32_t stage = sbuf + row * 128;
                 const int nsh = p.narrow_shift;   // heads narrower than 64: log2(d_k), else 0
-                const bool has_res = G.residual != nullptr && c.l0 + row < G.L;
-                const __nv_bfloat16* res_row =
-                    has_res ? G.residual + (static_cast<long>(c.b) * G.L + c.l0 + row) * p.N + n : nullptr;
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
                     uint32_t w[4];
-                    uint4 rv = make_uint4(0, 0, 0, 0);
-                    if (has_res) rv = *reinterpret_cast<const uint4*>(res_row + ch * 8);
-                    const __nv_bfloat162* r2 = reinterpret_cast<const __nv_bfloat162*>(&rv);
+                    const __nv_bfloat162* r2 = reinterpret_cast<const __nv_bfloat162*>(&res_cur[ch]);
                     const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&bias_cur[ch]);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -309,7 +320,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                             y0 = fmaxf(y0, 0.0f);
                             y1 = fmaxf(y1, 0.0f);
                         }
-                        if (has_res) {   // residual connection: x + sublayer(...)
+                        if (kRes) {   // residual connection: x + sublayer(...) (zeros past L)
                             const float2 rf = __bfloat1622float2(r2[e]);
                             y0 += rf.x;
                             y1 += rf.y;
@@ -338,7 +349,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                 }
                 ++slabs_issued;
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch) bias_cur[ch] = bias_next[ch];
+                for (int ch = 0; ch < 8; ++ch) {
+                    bias_cur[ch] = bias_next[ch];
+                    if constexpr (kRes) res_cur[ch] = res_next[ch];
+                }
             }
         }
         if (issuer) tma_store_wait_all();
@@ -362,7 +376,10 @@ size_t gemm_tc2_smem_bytes() { return kSmemBytes; }
 cudaError_t launch_gemm_tc2(const GemmParams& p, cudaStream_t s) {
     static_assert(kGemmBM == 128 && BN == 256, "epilogue assumes 128 x 256 tiles per CTA");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
-    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    bool res = false;
+    for (int g = 0; g < p.ngroups; ++g) res = res || p.g[g].residual != nullptr;
+    auto* kern = res ? gemm_bf16_tc2_kernel<true> : gemm_bf16_tc2_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
@@ -375,7 +392,7 @@ cudaError_t launch_gemm_tc2(const GemmParams& p, cudaStream_t s) {
         units += bn * ((p.g[g].L + 2 * kGemmBM - 1) / (2 * kGemmBM)) * n_tiles;
     }
     const long clusters = units < sms / 2 ? units : sms / 2;
-    return launch_pdl(gemm_bf16_tc2_kernel, dim3(static_cast<unsigned>(2 * clusters)), dim3(kGemmThreads),
+    return launch_pdl(kern, dim3(static_cast<unsigned>(2 * clusters)), dim3(kGemmThreads),
                       kSmemBytes, s, p);
 }
 
