@@ -72,6 +72,9 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, int tile, i
     return c;
 }
 
+// kRes: the instance for launches with a residual (the sublayer's W_o): each slab's residual
+// values are requested one slab ahead, like the bias; launches without one keep the lighter epilogue.
+template <bool kRes>
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -184,6 +187,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
             // slab's while the current one is converted: its load latency stays hidden
             uint4 bias_cur[8];
             load_bias_slab(G.bias, c.n0, p.N, bias_cur);
+            // this thread's output row of the residual (nullptr: none, or a row past L)
+            const __nv_bfloat16* res_row =
+                (kRes && G.residual != nullptr && c.l0 + row < G.L)
+                    ? G.residual + (static_cast<long>(c.b) * G.L + c.l0 + row) * p.N
+                    : nullptr;
+            uint4 res_cur[8];
+            if constexpr (kRes) load_residual_slab(res_row, c.n0, p.N, res_cur);
             mbar_wait(&sm->acc_full[acc], (use >> 1) & 1, abort_flag, p.status, 0x103);
             __syncwarp();
             tc_fence_after();
@@ -193,6 +203,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
                 const int n = c.n0 + slab * 64;
                 uint4 bias_next[8];
                 load_bias_slab(G.bias, slab + 1 < BN / 64 ? n + 64 : p.N, p.N, bias_next);
+                uint4 res_next[8];
+                if constexpr (kRes) load_residual_slab(res_row, slab + 1 < BN / 64 ? n + 64 : p.N, p.N, res_next);
                 uint32_t v[64];
                 tmem_ld_x64(t_row + slab * 64, v);
                 if (slab == BN / 64 - 1) {
@@ -202,7 +214,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
                 }
                 if (n >= p.N) {   // uniform across the CTA
 #pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) bias_cur[ch] = bias_next[ch];
+                    for (int ch = 0; ch < 8; ++ch) {
+                        bias_cur[ch] = bias_next[ch];
+                        if constexpr (kRes) res_cur[ch] = res_next[ch];
+                    }
                     continue;
                 }
                 const int sb = slabs_issued & 1;
@@ -212,15 +227,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
                 const uint32_t sbuf = smem_u32(base + kOffStage + sb * kSlabBytes);
                 const uint32_t stage = sbuf + row * 128;
                 const int nsh = p.narrow_shift;   // heads narrower than 64: log2(d_k), else 0
-                const bool has_res = G.residual != nullptr && c.l0 + row < G.L;
-                const __nv_bfloat16* res_row =
-                    has_res ? G.residual + (static_cast<long>(c.b) * G.L + c.l0 + row) * p.N + n : nullptr;
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
                     uint32_t w[4];
-                    uint4 rv = make_uint4(0, 0, 0, 0);
-                    if (has_res) rv = *reinterpret_cast<const uint4*>(res_row + ch * 8);
-                    const __nv_bfloat162* r2 = reinterpret_cast<const __nv_bfloat162*>(&rv);
+                    const __nv_bfloat162* r2 = reinterpret_cast<const __nv_bfloat162*>(&res_cur[ch]);
                     const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&bias_cur[ch]);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -232,7 +242,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
                             y0 = fmaxf(y0, 0.0f);
                             y1 = fmaxf(y1, 0.0f);
                         }
-                        if (has_res) {   // residual connection: x + sublayer(...)
+                        if (kRes) {   // residual connection: x + sublayer(...) (zeros past L)
                             const float2 rf = __bfloat1622float2(r2[e]);
                             y0 += rf.x;
                             y1 += rf.y;
@@ -261,7 +271,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
                 }
                 ++slabs_issued;
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch) bias_cur[ch] = bias_next[ch];
+                for (int ch = 0; ch < 8; ++ch) {
+                    bias_cur[ch] = bias_next[ch];
+                    if constexpr (kRes) res_cur[ch] = res_next[ch];
+                }
             }
         }
         if (issuer) tma_store_wait_all();
@@ -283,7 +296,10 @@ size_t gemm_tc_smem_bytes() { return kSmemBytes; }
 cudaError_t launch_gemm_tc(const GemmParams& p, int /*max_m_tiles*/, cudaStream_t s) {
     static_assert(kGemmBM == 128 && BN == 256, "epilogue assumes 128 x 256 tiles");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
-    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    bool res = false;
+    for (int g = 0; g < p.ngroups; ++g) res = res || p.g[g].residual != nullptr;
+    auto* kern = res ? gemm_bf16_tc_kernel<true> : gemm_bf16_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
@@ -293,7 +309,7 @@ cudaError_t launch_gemm_tc(const GemmParams& p, int /*max_m_tiles*/, cudaStream_
     long total = 0;
     for (int g = 0; g < p.ngroups; ++g) total += static_cast<long>(p.g[g].m_tiles) * n_tiles;
     const int grid = static_cast<int>(total < sms ? total : sms);
-    return launch_pdl(gemm_bf16_tc_kernel, dim3(grid), dim3(kGemmThreads), kSmemBytes, s, p);
+    return launch_pdl(kern, dim3(grid), dim3(kGemmThreads), kSmemBytes, s, p);
 }
 
 }  // namespace mha
