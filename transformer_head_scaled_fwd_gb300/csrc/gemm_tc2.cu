@@ -117,8 +117,10 @@ __device__ __forceinline__ int pair_units(const GemmParams& p, int n_tiles) {
 
 // kRes: the instance for launches with a residual (the sublayer's W_o): each slab's residual
 // values are requested one slab ahead, like the bias, so their load latency stays off the
-// epilogue's path; launches without one keep the lighter epilogue.
-template <bool kRes>
+// epilogue's path; launches without one keep the lighter epilogue. kRelu (the FFN's first layer)
+// and kNarrow (heads narrower than 64 in the head-split store) likewise compile their code only into
+// the instances that need it.
+template <bool kRes, bool kRelu, bool kNarrow>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_tc2_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -304,7 +306,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                 named_bar_sync(1, 128);
                 const uint32_t sbuf = smem_u32(base + kOffStage + sb * kSlabBytes);
                 const uint32_t stage = sbuf + row * 128;
-                const int nsh = p.narrow_shift;   // heads narrower than 64: log2(d_k), else 0
+                const int nsh = kNarrow ? p.narrow_shift : 0;   // heads narrower than 64: log2(d_k), else 0
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
                     uint32_t w[4];
@@ -316,7 +318,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                         const float2 bf = __bfloat1622float2(b2[e]);
                         float y0 = __uint_as_float(v[cc]) + bf.x;
                         float y1 = __uint_as_float(v[cc + 1]) + bf.y;
-                        if (p.relu) {
+                        if (kRelu) {
                             y0 = fmaxf(y0, 0.0f);
                             y1 = fmaxf(y1, 0.0f);
                         }
@@ -378,7 +380,12 @@ cudaError_t launch_gemm_tc2(const GemmParams& p, cudaStream_t s) {
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     bool res = false;
     for (int g = 0; g < p.ngroups; ++g) res = res || p.g[g].residual != nullptr;
-    auto* kern = res ? gemm_bf16_tc2_kernel<true> : gemm_bf16_tc2_kernel<false>;
+    // the instances the library launches: plain, ReLU (FFN layer 1), narrow heads (Q/K/V), residual (W_o)
+    auto* kern = gemm_bf16_tc2_kernel<false, false, false>;
+    if (p.relu && !res && !p.narrow_shift) kern = gemm_bf16_tc2_kernel<false, true, false>;
+    else if (p.narrow_shift && !res && !p.relu) kern = gemm_bf16_tc2_kernel<false, false, true>;
+    else if (res && !p.relu && !p.narrow_shift) kern = gemm_bf16_tc2_kernel<true, false, false>;
+    else if (res || p.relu || p.narrow_shift) return cudaErrorNotSupported;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
